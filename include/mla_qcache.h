@@ -1,0 +1,227 @@
+/*
+ * mla_qcache.h -- C ABI of the low-bit dual-path MLA KV cache for GB300 (sm_103a).
+ *
+ * Two operations make up the decode hot path of Multi-Head Latent Attention over a
+ * quantized, paged cache:
+ *
+ *   mla_qcache_write        fused cache writer: per-token latent quantize + pack, BF16
+ *                           retention of sink and recent tokens, and per-page k_R
+ *                           quantization once a page fills.
+ *   mla_qcache_decode_attn  single-token decode attention over the packed pages plus the
+ *                           BF16 protected tokens, one global softmax, latent-space readout.
+ *
+ * Sources (the web pages this library follows):
+ *   [QuantMLA]  the QuantMLA page (function-aligned dual-path quantization of MLA caches):
+ *               abstract (native low-bit kernel that unpacks and dequantizes inside
+ *               attention), Figure 3 caption (packed cache plus BF16 sink/recent buffers),
+ *               Figure 5 caption (C4R4 with sink4/local128), appendix Figure 8 caption
+ *               (fused writer, switch to the packed copy on eviction, one global softmax).
+ *   [RAQ-MLA]   the RAQ-MLA page (Role-Aware Quantization for Multi-Head Latent Attention
+ *               Caches): abstract and Figures 3-4 (what is cached: latent c_KV and post-RoPE k_R;
+ *               absorbed read path), appendix Table 5 (quantizer configuration), appendix
+ *               Table 6 (cache page of 64 or 128 tokens).
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers unless stated otherwise. The caller owns every
+ *     buffer; the library allocates nothing and never synchronizes the stream.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Work is
+ *     enqueued asynchronously on it.
+ *   - BF16 values are passed as their 16-bit patterns (uint16_t), FP16 metadata likewise.
+ *   - The synchronous return value is a status (MLA_QCACHE_OK or a negative MLA_QCACHE_ERR_*).
+ *     On a negative status nothing was enqueued.
+ *   - Problems that can only be seen on the device (bad page id, overflowing sequence,
+ *     non-finite input, ...) are OR-ed into *err_word (a device int32 that the caller zeroes
+ *     and reads after synchronizing) as MLA_QCACHE_DEV_* bits. The offending work is skipped;
+ *     kernels never trap.
+ */
+#ifndef MLA_QCACHE_H
+#define MLA_QCACHE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Fixed MLA dimensions ([RAQ-MLA] Table 5; DeepSeek-V2/GLM-shaped MLA). */
+#define MLA_QCACHE_LATENT_DIM 512 /* rank of the compressed latent c_KV */
+#define MLA_QCACHE_ROPE_DIM 64    /* dimension of the post-RoPE positional key k_R */
+#define MLA_QCACHE_GROUP 128      /* latent channels per quantization group */
+#define MLA_QCACHE_ROW_DIM 576    /* one BF16 buffer row: c (512) followed by k_R (64) */
+
+/* Synchronous status codes. */
+#define MLA_QCACHE_OK 0
+#define MLA_QCACHE_ERR_NULL (-1)      /* a required pointer is NULL */
+#define MLA_QCACHE_ERR_CONFIG (-2)    /* unsupported configuration (bits, page, sink, recent) */
+#define MLA_QCACHE_ERR_SHAPE (-3)     /* bad B, H, row count, max_pages, n_pages, max_new */
+#define MLA_QCACHE_ERR_ALIGN (-4)     /* a pointer is not aligned as documented */
+#define MLA_QCACHE_ERR_WORKSPACE (-5) /* workspace too small */
+#define MLA_QCACHE_ERR_CUDA (-6)      /* a CUDA runtime call failed (launch, attribute, ...) */
+
+/* Device-side error bits, OR-ed into *err_word. */
+#define MLA_QCACHE_DEV_BAD_PAGE 1      /* page-table entry outside [0, n_pages) */
+#define MLA_QCACHE_DEV_SEQ_OVERFLOW 2  /* a position >= max_pages * page_size, or seq_len < 0 */
+#define MLA_QCACHE_DEV_NONFINITE 4     /* NaN or Inf in a value to quantize */
+#define MLA_QCACHE_DEV_RANGE 8         /* a group min/max outside the finite FP16 range */
+#define MLA_QCACHE_DEV_ROWS 16         /* cu_new inconsistent with n_rows or max_new */
+#define MLA_QCACHE_DEV_TIMEOUT 32      /* a bounded device wait expired (work abandoned) */
+
+/*
+ * Cache configuration.
+ *   bits_c     latent code width: 4 (C4) or 2 (C2). 2^bits_c levels, L = 2^bits_c - 1.
+ *   bits_r     k_R code width: must be 4 (R4).
+ *   page_size  P, tokens per cache page: 16, 32, 64 or 128, and P <= n_recent.
+ *   n_sink     S, leading tokens kept in BF16 ("sink4"): 0..16.
+ *   n_recent   W, trailing tokens kept in BF16 ("local128"): P..1024.
+ *   clip_q     per-token clip quantile of |c| for the latent, in (0, 1]; 0 disables the clip.
+ *              [RAQ-MLA] Table 5 lists a 0.94 clip under the INT2 latent.
+ *
+ * Quantizer ([RAQ-MLA] Table 5; the exact roundings are this library's reading, since the
+ * pages only say "FP16 scale and minimum"). For a set of values x (one latent group of 128
+ * channels of one token, or one k_R channel over the P tokens of one page):
+ *   lo = min x, hi = max x
+ *   min   = the largest finite FP16 value <= lo                  (round down)
+ *   scale = the smallest FP16 value >= 0 with min + L*scale >= hi (round up of (hi-min)/L)
+ *   code(x) = the k in [0, L] minimising |x - (min + k*scale)|, exact ties to the even k
+ *   dequantized value: min + code * scale
+ * so |dequant - x| <= scale/2 holds exactly. Clip (latent only, when clip_q > 0): tau is the
+ * k-th smallest |c_i| over the 512 channels of the token with k = ceil(clip_q * 512) (a
+ * nearest-rank order statistic), and each c_i is replaced by min(max(c_i, -tau), tau) before
+ * the group statistics.
+ */
+typedef struct {
+  int32_t bits_c;
+  int32_t bits_r;
+  int32_t page_size;
+  int32_t n_sink;
+  int32_t n_recent;
+  float clip_q;
+} mla_qcache_config;
+
+/*
+ * Physical page layout (this library's own; the pages say only "packed cache
+ * representations" and give no byte layout). One contiguous region of
+ * mla_qcache_page_bytes() bytes per physical page of P tokens; t is the token's index in
+ * its page (position mod P), c a latent channel (0..511), j a k_R channel (0..63).
+ *
+ *   Region A, latent codes, offset 0, size P*64*bits_c bytes.
+ *     Blocks of 8 tokens x 128 channels (one group g = c/128): block (t/8, g) starts at
+ *     ((t/8)*4 + g) * 128*bits_c. A block is 32 lanes of 4*bits_c bytes, lane = 4*(t%8) + q,
+ *     each lane a run of bits_c little-endian 32-bit words. With cc = c%128,
+ *     k = cc/16, e = cc%16, q = (e%8)/2, h = e/8, o = e%2:
+ *       bits_c == 4: word k/2, field s = 2*(k%2) + h, bits [4*(s+4*o), 4*(s+4*o)+4)
+ *       bits_c == 2: word k/4, field s = 2*(k%4) + h, bits [2*(s+8*o), 2*(s+8*o)+2)
+ *     (So shifting a word right by 4*s (or 2*s) and masking the low field of each 16-bit
+ *     half yields channels (2q, 2q+1) or (2q+8, 2q+9) of one 16-channel chunk of token t%8:
+ *     the B operand of a 16x8x16 tensor-core product with tokens as columns.)
+ *   Region B, k_R codes (4 bits), offset P*64*bits_c, size 32*P bytes.
+ *     Blocks of 16 tokens x 16 channels: block (t/16, j/16) starts at ((t/16)*4 + j/16)*128.
+ *     A block is 32 lanes of one 32-bit word, lane = 4*(t%8) + q. With e = j%16,
+ *     q = (e%8)/2, h = e/8, o = e%2, n = (t%16)/8: field s = 2*n + h, bits [4*(s+4*o), +4).
+ *   Region C, latent metadata, offset P*(64*bits_c + 32), size 16*P bytes.
+ *     Token t, group g at (t*4 + g)*4: FP16 scale (2 bytes) then FP16 minimum (2 bytes).
+ *   Region D, k_R metadata, offset P*(64*bits_c + 48), size 256 bytes.
+ *     Channel j at j*4: FP16 scale then FP16 minimum, over the P tokens of the page.
+ *
+ *   Effective bits ([RAQ-MLA] Table 5): latent (64*bits_c + 16)*8/512 = 2.25 (C2) or 4.25
+ *   (C4) bits/element; k_R (32*P + 256)*8/(64*P) = 4 + 32/P = 4.25 (P=128) or 4.50 (P=64).
+ *
+ * BF16 buffers ([QuantMLA] Figure 8): sink_buf [B][n_sink][576] holds positions 0..S-1;
+ * recent_buf [B][n_recent][576] is a ring, position t in slot t % W. A row is c (512) then
+ * k_R (64), the pre-quantization (unclipped) values.
+ *
+ * Which tokens attention reads from BF16 ("protected"), for a sequence of T cached tokens:
+ * t < S or t >= T - W. Every other token is read from its packed copy. Because P <= W, a
+ * token that is not protected lies in a full page whose k_R is already quantized.
+ */
+
+/* Bytes of one physical page, or 0 for an invalid configuration. */
+size_t mla_qcache_page_bytes(const mla_qcache_config* cfg);
+
+/* MLA_QCACHE_OK if the configuration is supported, else MLA_QCACHE_ERR_CONFIG/NULL. */
+int mla_qcache_config_check(const mla_qcache_config* cfg);
+
+/*
+ * Bytes of device workspace mla_qcache_decode_attn needs for B sequences, H heads and a
+ * page table of max_pages columns (the split of the KV axis depends on these and on the
+ * SM count of the current device). Returns 0 on invalid arguments.
+ */
+size_t mla_qcache_workspace_bytes(const mla_qcache_config* cfg, int32_t B, int32_t H,
+                                  int32_t max_pages);
+
+/*
+ * Fused cache writer ([QuantMLA] Figure 8; [RAQ-MLA] Table 5).
+ *
+ * For each sequence b in [0, B), rows cu_new[b] .. cu_new[b+1]-1 of c_new / kr_new are the
+ * new tokens at positions seq_lens[b], seq_lens[b]+1, ... (seq_lens[b] = tokens already
+ * cached before this call; the caller advances it afterwards). For every new token t:
+ *   - the latent is clipped (if clip_q > 0), quantized per 128-channel group and its codes
+ *     and metadata are stored in page page_table[b][t/P], slot t%P (regions A and C);
+ *   - if t < S, its BF16 row is stored in sink_buf[b][t];
+ *   - if t is among the last W positions after this call, its BF16 row is stored in
+ *     recent_buf[b][t%W] (earlier rows of this call would be overwritten anyway);
+ *   - if t is the last token of its page, the page's k_R is quantized per channel over the
+ *     page's P tokens (regions B and D), reading earlier tokens of the page from the ring.
+ * A token leaving the recent window needs no work: its packed copy already exists.
+ *
+ * Arguments:
+ *   c_new      [n_rows][512] BF16, kr_new [n_rows][64] BF16 (post-RoPE), row-major.
+ *   cu_new     [B+1] int32, non-decreasing, cu_new[0] = 0, cu_new[B] = n_rows.
+ *   seq_lens   [B] int32, tokens cached before this call.
+ *   max_new    host int: upper bound on cu_new[b+1]-cu_new[b] (1 for a decode step).
+ *   page_table [B][max_pages] int32 physical page ids; entries for every position written
+ *              must be valid (the caller allocates pages before writing into them).
+ *   pool       [n_pages][page_bytes] bytes, 16-byte aligned.
+ *   sink_buf   [B][S][576] BF16 (may be NULL when S == 0); recent_buf [B][W][576] BF16.
+ *   err_word   device int32 receiving MLA_QCACHE_DEV_* bits (required).
+ * Errors: NULL pointer, bad config, B < 1, n_rows < 0, max_new < 1 (with n_rows > 0),
+ * max_pages < 1, n_pages < 1, misaligned pool or buffers -> negative status, nothing run.
+ */
+int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows,
+                     const uint16_t* c_new, const uint16_t* kr_new, const int32_t* cu_new,
+                     const int32_t* seq_lens, int32_t max_new, const int32_t* page_table,
+                     int32_t max_pages, uint8_t* pool, int64_t n_pages, uint16_t* sink_buf,
+                     uint16_t* recent_buf, int32_t* err_word, void* stream);
+
+/*
+ * Decode attention over the quantized dual-path cache ([QuantMLA] abstract and Figure 8;
+ * [RAQ-MLA] Figures 3-4: absorbed query, score = q_lat . c + q_rope . k_R, latent-space
+ * readout).
+ *
+ * For each sequence b with T = seq_lens[b] cached tokens and each head h:
+ *   v_t   = BF16 row of token t if protected (t < S or t >= T-W), else its dequantized
+ *           packed copy (latent codes with the token's group metadata, k_R codes with the
+ *           page's channel metadata)
+ *   s_t   = softmax_scale * (q_lat[b][h] . v_t[0:512] + q_rope[b][h] . v_t[512:576])
+ *   out[b][h][:] = sum_t exp(s_t - m) v_t[0:512] / sum_t exp(s_t - m),  m = max_t s_t
+ *   lse[b][h]    = m + ln(sum_t exp(s_t - m))   (natural log; -inf and out = 0 when T = 0)
+ * All tokens share one softmax normalization.
+ *
+ * Arguments:
+ *   H          heads: a multiple of 16, 16..256.
+ *   q_lat      [B][H][512] BF16 absorbed query, q_rope [B][H][64] BF16.
+ *   page_table [B][max_pages] int32, seq_lens [B] int32 (0 <= T <= max_pages * P).
+ *   pool, sink_buf, recent_buf as written by mla_qcache_write.
+ *   out        [B][H][512] float32, lse [B][H] float32.
+ *   workspace  device scratch of at least mla_qcache_workspace_bytes(cfg, B, H, max_pages)
+ *              bytes, 256-byte aligned; it needs no initialization and its contents are
+ *              meaningless after the call. Calls sharing one workspace must not overlap.
+ * Errors: as for the writer, plus H not a multiple of 16 or > 256, workspace too small.
+ */
+int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H,
+                           const uint16_t* q_lat, const uint16_t* q_rope,
+                           const int32_t* page_table, int32_t max_pages,
+                           const int32_t* seq_lens, const uint8_t* pool, int64_t n_pages,
+                           const uint16_t* sink_buf, const uint16_t* recent_buf,
+                           float softmax_scale, float* out, float* lse, void* workspace,
+                           size_t workspace_bytes, int32_t* err_word, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* mla_qcache_strerror(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_QCACHE_H */

@@ -1,0 +1,223 @@
+"""Oracle for the low-bit dual-path MLA KV cache (test infrastructure only).
+
+A plain fp64 CPU restatement, in C (``oracle.c``), of the fused cache writer and the decode
+attention, following the RAQ-MLA page (appendix Table 5: the quantizer; Figures 3-4: the
+dual-path read) and the QuantMLA page (appendix Figure 8: the fused writer, BF16 protection
+of sink and recent tokens, one global softmax). See ``oracle.c`` for the readings taken where
+the pages are silent.
+
+Only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline / reference legs
+may import this package. It shares no code with the CUDA library and never imports it.
+
+Parity status: every function here is pinned by ``tests/test_oracle_*.py`` against values
+that do not come from the oracle itself (numpy's float16, exact rational brute force, the
+effective-bits figures of Table 5, closed forms of softmax attention, and
+``torch.nn.functional.scaled_dot_product_attention`` in float64).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+
+LATENT, ROPE, ROW, GROUP = 512, 64, 576, 128
+
+ERR_BAD_PAGE, ERR_SEQ_OVERFLOW, ERR_NONFINITE, ERR_RANGE, ERR_ROWS = 1, 2, 4, 8, 16
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (plain gcc, no GPU code)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        cmd = ["gcc", "-std=c11", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+               "-shared", "-fPIC", "-o", _LIB_PATH, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+    return _LIB_PATH
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("bits_c", ctypes.c_int32), ("bits_r", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("n_sink", ctypes.c_int32),
+                ("n_recent", ctypes.c_int32), ("clip_q", ctypes.c_float)]
+
+
+def make_config(bits_c=4, page_size=128, n_sink=4, n_recent=128, clip_q=None, bits_r=4) -> Config:
+    if clip_q is None:
+        clip_q = 0.94 if bits_c == 2 else 0.0
+    return Config(bits_c, bits_r, page_size, n_sink, n_recent, clip_q)
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(build())
+        P = ctypes.POINTER
+        d, i32, u8, u16 = ctypes.c_double, ctypes.c_int32, ctypes.c_uint8, ctypes.c_uint16
+        _lib.oracle_bf16_to_double.restype = d
+        _lib.oracle_bf16_to_double.argtypes = [u16]
+        _lib.oracle_f16_to_double.restype = d
+        _lib.oracle_f16_to_double.argtypes = [u16]
+        _lib.oracle_f16_bits.restype = u16
+        _lib.oracle_f16_bits.argtypes = [d]
+        _lib.oracle_f16_round_down.restype = d
+        _lib.oracle_f16_round_down.argtypes = [d, P(ctypes.c_int)]
+        _lib.oracle_f16_round_up.restype = d
+        _lib.oracle_f16_round_up.argtypes = [d, P(ctypes.c_int)]
+        _lib.oracle_quantize.restype = ctypes.c_int
+        _lib.oracle_quantize.argtypes = [P(d), ctypes.c_int, ctypes.c_int, P(u8), P(u16), P(u16)]
+        _lib.oracle_clip_tau.restype = d
+        _lib.oracle_clip_tau.argtypes = [P(d), ctypes.c_int, ctypes.c_float]
+        _lib.oracle_page_bytes.restype = ctypes.c_size_t
+        _lib.oracle_page_bytes.argtypes = [P(Config)]
+        _lib.oracle_config_ok.restype = ctypes.c_int
+        _lib.oracle_config_ok.argtypes = [P(Config)]
+        _lib.oracle_latent_code_pos.restype = None
+        _lib.oracle_latent_code_pos.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                P(ctypes.c_size_t), P(ctypes.c_int)]
+        _lib.oracle_rope_code_pos.restype = None
+        _lib.oracle_rope_code_pos.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              P(ctypes.c_size_t), P(ctypes.c_int)]
+        _lib.oracle_write.restype = ctypes.c_int
+        _lib.oracle_write.argtypes = [P(Config), ctypes.c_int, ctypes.c_int, P(u16), P(u16), P(i32),
+                                      P(i32), ctypes.c_int, P(i32), ctypes.c_int, P(u8),
+                                      ctypes.c_int64, P(u16), P(u16)]
+        _lib.oracle_token_values.restype = ctypes.c_int
+        _lib.oracle_token_values.argtypes = [P(Config), ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             P(i32), ctypes.c_int, P(u8), ctypes.c_int64, P(u16),
+                                             P(u16), P(d)]
+        _lib.oracle_decode.restype = ctypes.c_int
+        _lib.oracle_decode.argtypes = [P(Config), ctypes.c_int, ctypes.c_int, P(u16), P(u16), P(i32),
+                                       ctypes.c_int, P(i32), P(u8), ctypes.c_int64, P(u16), P(u16),
+                                       ctypes.c_float, P(d), P(d)]
+    return _lib
+
+
+def _ptr(a: np.ndarray, ctype):
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+# ------------------------------------------------------------------ number formats
+
+def bf16_to_double(bits: int) -> float:
+    return lib().oracle_bf16_to_double(int(bits))
+
+
+def f16_to_double(bits: int) -> float:
+    return lib().oracle_f16_to_double(int(bits))
+
+
+def f16_bits(v: float) -> int:
+    return int(lib().oracle_f16_bits(float(v)))
+
+
+def f16_round_down(x: float):
+    r = ctypes.c_int(0)
+    v = lib().oracle_f16_round_down(float(x), ctypes.byref(r))
+    return v, bool(r.value)
+
+
+def f16_round_up(x: float):
+    r = ctypes.c_int(0)
+    v = lib().oracle_f16_round_up(float(x), ctypes.byref(r))
+    return v, bool(r.value)
+
+
+# ------------------------------------------------------------------ quantizer
+
+def quantize(x, bits: int):
+    """Returns (codes uint8[n], scale_bits, min_bits, flags)."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    codes = np.zeros(x.shape[0], dtype=np.uint8)
+    sb, mb = ctypes.c_uint16(0), ctypes.c_uint16(0)
+    fl = lib().oracle_quantize(_ptr(x, ctypes.c_double), x.shape[0], bits, _ptr(codes, ctypes.c_uint8),
+                               ctypes.byref(sb), ctypes.byref(mb))
+    return codes, int(sb.value), int(mb.value), int(fl)
+
+
+def clip_tau(x, clip_q: float) -> float:
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    return lib().oracle_clip_tau(_ptr(x, ctypes.c_double), x.shape[0], ctypes.c_float(clip_q))
+
+
+# ------------------------------------------------------------------ layout
+
+def page_bytes(cfg: Config) -> int:
+    return int(lib().oracle_page_bytes(ctypes.byref(cfg)))
+
+
+def config_ok(cfg: Config) -> bool:
+    return bool(lib().oracle_config_ok(ctypes.byref(cfg)))
+
+
+def latent_code_pos(bits_c: int, t: int, c: int):
+    b, s = ctypes.c_size_t(0), ctypes.c_int(0)
+    lib().oracle_latent_code_pos(bits_c, t, c, ctypes.byref(b), ctypes.byref(s))
+    return int(b.value), int(s.value)
+
+
+def rope_code_pos(bits_c: int, page_size: int, t: int, j: int):
+    b, s = ctypes.c_size_t(0), ctypes.c_int(0)
+    lib().oracle_rope_code_pos(bits_c, page_size, t, j, ctypes.byref(b), ctypes.byref(s))
+    return int(b.value), int(s.value)
+
+
+# ------------------------------------------------------------------ writer / reader / decode
+
+def write(cfg: Config, c_new, kr_new, cu_new, seq_lens, max_new, page_table, pool, sink, ring) -> int:
+    """In-place sequential writer over numpy buffers; returns ERR_* flags."""
+    c_new = np.ascontiguousarray(c_new, dtype=np.uint16)
+    kr_new = np.ascontiguousarray(kr_new, dtype=np.uint16)
+    cu_new = np.ascontiguousarray(cu_new, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    page_table = np.ascontiguousarray(page_table, dtype=np.int32)
+    for a in (pool, sink, ring):
+        assert a.flags["C_CONTIGUOUS"]
+    B = seq_lens.shape[0]
+    n_rows = c_new.shape[0]
+    sink_arg = sink if sink.size else np.zeros(1, dtype=np.uint16)
+    return int(lib().oracle_write(ctypes.byref(cfg), B, n_rows, _ptr(c_new, ctypes.c_uint16),
+                                  _ptr(kr_new, ctypes.c_uint16), _ptr(cu_new, ctypes.c_int32),
+                                  _ptr(seq_lens, ctypes.c_int32), int(max_new),
+                                  _ptr(page_table, ctypes.c_int32), page_table.shape[1],
+                                  _ptr(pool, ctypes.c_uint8), pool.shape[0],
+                                  _ptr(sink_arg, ctypes.c_uint16), _ptr(ring, ctypes.c_uint16)))
+
+
+def token_values(cfg: Config, b: int, t: int, T: int, page_table, pool, sink, ring):
+    """(values float64[576], status): status 1 = BF16 row, 0 = dequantized packed copy."""
+    v = np.zeros(ROW, dtype=np.float64)
+    page_table = np.ascontiguousarray(page_table, dtype=np.int32)
+    sink_arg = sink if sink.size else np.zeros(1, dtype=np.uint16)
+    st = lib().oracle_token_values(ctypes.byref(cfg), b, t, T, _ptr(page_table, ctypes.c_int32),
+                                   page_table.shape[1], _ptr(pool, ctypes.c_uint8), pool.shape[0],
+                                   _ptr(sink_arg, ctypes.c_uint16), _ptr(ring, ctypes.c_uint16),
+                                   _ptr(v, ctypes.c_double))
+    return v, int(st)
+
+
+def decode(cfg: Config, q_lat, q_rope, page_table, seq_lens, pool, sink, ring, softmax_scale: float):
+    """Returns (out float64[B,H,512], lse float64[B,H], flags)."""
+    q_lat = np.ascontiguousarray(q_lat, dtype=np.uint16)
+    q_rope = np.ascontiguousarray(q_rope, dtype=np.uint16)
+    page_table = np.ascontiguousarray(page_table, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, H = q_lat.shape[0], q_lat.shape[1]
+    out = np.zeros((B, H, LATENT), dtype=np.float64)
+    lse = np.zeros((B, H), dtype=np.float64)
+    sink_arg = sink if sink.size else np.zeros(1, dtype=np.uint16)
+    fl = lib().oracle_decode(ctypes.byref(cfg), B, H, _ptr(q_lat, ctypes.c_uint16),
+                             _ptr(q_rope, ctypes.c_uint16), _ptr(page_table, ctypes.c_int32),
+                             page_table.shape[1], _ptr(seq_lens, ctypes.c_int32),
+                             _ptr(pool, ctypes.c_uint8), pool.shape[0], _ptr(sink_arg, ctypes.c_uint16),
+                             _ptr(ring, ctypes.c_uint16), ctypes.c_float(softmax_scale),
+                             _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    return out, lse, int(fl)
