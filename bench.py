@@ -1,0 +1,451 @@
+"""Benchmark of the low-bit dual-path MLA decode hot path on one GB300 (one JSON line).
+
+A step is one decode step of one layer: the fused writer appends one token to every sequence
+of the layer's cache, then decode attention reads the whole cache (packed pages + BF16
+protected tokens) for every head. Steps rotate over several layer caches whose total size is
+several times the L2 cache, so every step streams its cache from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+--impl reference times the fp64 CPU oracle (the reference arm of this build) on the host.
+Under torchrun (N > 1) every rank runs an independent replica over its own sequences (the path
+shards by sequence with no exchange); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "decode attn µs/layer and packed-cache HBM GB/s (fraction of 8 TB/s) on 1 GB300"
+DEFAULT_WORKLOAD = "v2lite_c4r4_b32_h16_t8k"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--layers", type=int, default=0, help="layer caches rotated (0 = enough for 3x L2)")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ algorithmic work per step
+
+def decode_bytes(w: workloads.Workload, seq_lens, heads) -> int:
+    """Bytes the method must move per decode call: packed copies of unprotected tokens
+    (codes + per-token group metadata + per-page k_R metadata), BF16 rows of protected tokens,
+    the queries and the outputs."""
+    P, S, W = w.page_size, w.n_sink, w.n_recent
+    per_tok = 64 * w.bits_c + 32 + 16  # latent codes + k_R codes + latent metadata
+    total = 0
+    for T in seq_lens:
+        T = int(T)
+        prot = min(T, S) + max(0, T - max(T - W, min(T, S)))
+        packed = T - prot
+        pages = math.ceil(max(T - W, 0) / P) if packed else 0
+        total += packed * per_tok + pages * 256 + prot * 576 * 2
+    B = len(seq_lens)
+    total += B * heads * 576 * 2 + B * heads * (512 + 1) * 4
+    return total
+
+
+def decode_flops(seq_lens, heads) -> int:
+    return int(sum(int(T) for T in seq_lens)) * heads * 2 * (576 + 512)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_mla_kv_qcache_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per decode call from the committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m_sha = re.search(r"source_sha:\s*([0-9a-f]+)", txt)
+    m_b = re.search(r"dram_bytes_per_call:\s*([0-9.e+]+)", txt)
+    if not m_sha or not m_b or m_sha.group(1) != source_sha():
+        return None
+    return float(m_b.group(1))
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline / reference arm)
+
+def oracle_step_sample(w: workloads.Workload, n_seq: int):
+    """Build an oracle cache for n_seq sequences; return a closure that times one sampled step
+    (write one token per sampled sequence + decode those sequences) and the scale factor to one
+    full step of the workload."""
+    import oracle
+    n_seq = max(1, min(n_seq, w.batch))
+    lens = workloads.seq_lens_for(w)[:n_seq]
+    inp = workloads.make_inputs(w, seq_lens=lens, extra_pages=1)
+    cfg = oracle.make_config(**w.config_kwargs())
+    pool = np.zeros((inp.n_pages, oracle.page_bytes(cfg)), np.uint8)
+    sink = np.zeros((n_seq, cfg.n_sink, 576), np.uint16)
+    ring = np.zeros((n_seq, cfg.n_recent, 576), np.uint16)
+    oracle.write(cfg, inp.c, inp.kr, inp.cu, np.zeros(n_seq, np.int32), int(lens.max()), inp.page_table, pool, sink,
+                 ring)
+    rng = np.random.default_rng(123)
+    state = {"lens": lens.astype(np.int32).copy()}
+
+    def step():
+        c1, k1 = workloads.draw_tokens(rng, n_seq, w.latent_dist, inp.outliers, w.outlier_scale)
+        t0 = time.perf_counter()
+        oracle.write(cfg, c1, k1, np.arange(n_seq + 1, dtype=np.int32), state["lens"], 1, inp.page_table, pool, sink,
+                     ring)
+        state["lens"] = state["lens"] + 1
+        oracle.decode(cfg, inp.q_lat, inp.q_rope, inp.page_table, state["lens"], pool, sink, ring, w.softmax_scale)
+        return time.perf_counter() - t0
+
+    return step, w.batch / n_seq
+
+
+def cpu_cores() -> int:
+    if os.environ.get("OMP_NUM_THREADS"):
+        return int(os.environ["OMP_NUM_THREADS"])
+    return os.cpu_count() or 1
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    n_seq = max(1, w.batch // 16)
+    step, scale = oracle_step_sample(w, n_seq)
+    for _ in range(max(0, min(args.warmup, 1))):
+        step()
+    times = [step() for _ in range(args.steps)]
+    us = statistics.mean(times) * scale * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": "us/layer", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w, 0),
+        "cpu_baseline": {"value": us, "unit": "us/layer", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"oracle write of 1 token + decode for {n_seq} of {w.batch} sequences per step, "
+                                   f"scaled x{scale:g} to the full batch"},
+        "e2e": {"value": us, "unit": "us/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def config_dict(w, layers):
+    return {"workload": w.name, "batch": w.batch, "heads": w.heads, "seq_len": w.seq_len,
+            "cache": f"C{w.bits_c}R4", "page": w.page_size, "sink": w.n_sink, "recent": w.n_recent,
+            "clip_q": w.clip_q, "layers_rotated": layers,
+            "l2": "inputs larger than L2: each step reads a layer cache last touched layers_rotated-1 steps earlier"}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_native(args, w):
+    import torch
+
+    import bit_mla_kv_qcache_gb300 as q
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = q.make_config(**w.config_kwargs())
+    B, H = w.batch, w.heads
+
+    steps_total = args.warmup + args.steps + 8
+    inp = workloads.make_inputs(w, extra_pages=math.ceil(steps_total / w.page_size) + 1)
+    max_pages = inp.page_table.shape[1]
+    per_layer = inp.n_pages * q.page_bytes(cfg)
+    NL = args.layers or max(2, math.ceil(3 * L2_BYTES / per_layer) + 1)
+
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else
+                                   np.ascontiguousarray(a)).to(dev)
+    pt = t(inp.page_table)
+    c_all, kr_all, cu_all = t(inp.c), t(inp.kr), t(inp.cu)
+    caches = []
+    for _ in range(NL):
+        cache = q.QuantizedMLACache(cfg, B, max_pages, inp.n_pages, page_table=pt, device=dev)
+        cache.write(c_all, kr_all, cu_all, int(inp.seq_lens.max()))
+        caches.append(cache)
+    del c_all, kr_all
+    torch.cuda.synchronize()
+    if any(c.error_bits() for c in caches):
+        raise RuntimeError("writer reported device errors during prefill")
+
+    # per-step inputs: one new token per sequence, queries (fixed across steps)
+    rng = np.random.default_rng(1234)
+    c1, k1 = workloads.draw_tokens(rng, B, w.latent_dist, inp.outliers, w.outlier_scale)
+    c_new, kr_new = t(c1), t(k1)
+    cu1 = torch.arange(B + 1, dtype=torch.int32, device=dev)
+    q_lat, q_rope = t(inp.q_lat), t(inp.q_rope)
+    out = torch.empty((B, H, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    ws_buf = caches[0].workspace(H)
+    one = torch.ones(B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def write_step(cache):
+        q.mla_qcache_write(cfg, c_new, kr_new, cu1, cache.seq_lens, 1, cache.page_table, cache.pool, cache.sink,
+                           cache.ring, cache.err)
+        cache.seq_lens.add_(one)
+
+    def decode_step(cache):
+        q.mla_qcache_decode_attn(cfg, q_lat, q_rope, cache.page_table, cache.seq_lens, cache.pool, cache.sink,
+                                 cache.ring, w.softmax_scale, out, lse, ws_buf, cache.err)
+
+    # capture one graph per layer for the writer and for the decode (launch overhead off the path)
+    g_write, g_dec = [], []
+    with torch.cuda.stream(stream):
+        for cache in caches:  # warm the code paths once before capture
+            decode_step(cache)
+        torch.cuda.synchronize()
+        for cache in caches:
+            gw, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gw, stream=stream):
+                write_step(cache)
+            with torch.cuda.graph(gd, stream=stream):
+                decode_step(cache)
+            g_write.append(gw)
+            g_dec.append(gd)
+    torch.cuda.synchronize()
+
+    head_start = torch.empty(int(1.5e9) // 4, dtype=torch.float32, device=dev)  # lets the host queue ahead
+
+    def run(K, events=None):
+        for k in range(K):
+            L = k % NL
+            g_write[L].replay()
+            if events is not None:
+                events[k][0].record(stream)
+            g_dec[L].replay()
+            if events is not None:
+                events[k][1].record(stream)
+
+    with torch.cuda.stream(stream):
+        run(args.warmup)
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        seq_before = caches[0].seq_lens.cpu().numpy().copy()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clk:
+            head_start.fill_(1.0)
+            start.record(stream)
+            run(args.steps, ev)
+            end.record(stream)
+            torch.cuda.synchronize()
+        total_ms = start.elapsed_time(end)
+        dec_ms = [a.elapsed_time(b) for a, b in ev]
+    if ws > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    if any(c.error_bits() for c in caches):
+        raise RuntimeError("device error bits set during the timed region")
+
+    us_step = total_ms * 1e3 / args.steps
+    dec_us = statistics.mean(dec_ms) * 1e3
+    # sequence lengths seen by the timed decodes (grow by one per layer visit)
+    mean_T = seq_before + (args.steps / NL) / 2 + 1
+    bytes_dec = decode_bytes(w, mean_T, H)
+    flops_dec = decode_flops(mean_T, H)
+    hbm_peak, peak_kind = peaks()
+    achieved = bytes_dec / (dec_us * 1e-6) / 1e9
+    traffic = profiled_traffic(w.name)
+
+    result = {
+        "metric": METRIC, "value": us_step * 1.0, "unit": "us/layer", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us_step / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(w, NL),
+        "decode_us": dec_us, "write_us": max(0.0, us_step - dec_us),
+        "packed_cache_gbs": achieved, "fraction_of_8tbs": achieved / 8000.0,
+        "decode_tflops": flops_dec / (dec_us * 1e-6) / 1e12,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic,
+                     "kernel": "mla_qcache_decode_attn (decode_kernel + combine_kernel)",
+                     "algorithmic_bytes_per_call": bytes_dec, "peak_kind": peak_kind},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = e2e_measure(args, w, q, caches[0], cfg, inp, dev)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(result))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def e2e_measure(args, w, q, cache, cfg, inp, dev):
+    """Same step through the public API from pinned host buffers: H2D of the step's new tokens
+    and queries, write + decode, D2H of O and LSE, all inside the timed region."""
+    import torch
+    B, H = w.batch, w.heads
+    rng = np.random.default_rng(99)
+    c1, k1 = workloads.draw_tokens(rng, B, w.latent_dist, inp.outliers, w.outlier_scale)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
+    h_c, h_k, h_ql, h_qr = pin(c1), pin(k1), pin(inp.q_lat), pin(inp.q_rope)
+    h_out = torch.empty((B, H, 512), dtype=torch.float32).pin_memory()
+    h_lse = torch.empty((B, H), dtype=torch.float32).pin_memory()
+    d_c, d_k = torch.empty_like(h_c, device=dev), torch.empty_like(h_k, device=dev)
+    d_ql, d_qr = torch.empty_like(h_ql, device=dev), torch.empty_like(h_qr, device=dev)
+    cu1 = torch.arange(B + 1, dtype=torch.int32, device=dev)
+    out = torch.empty((B, H, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    K = max(10, args.steps // 2)
+
+    def step():
+        d_c.copy_(h_c, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_ql.copy_(h_ql, non_blocking=True)
+        d_qr.copy_(h_qr, non_blocking=True)
+        cache.write(d_c, d_k, cu1, 1)
+        cache.decode(d_ql, d_qr, w.softmax_scale, out=out, lse=lse)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(K):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    us = s.elapsed_time(e) * 1e3 / K
+    h2d = sum(x.numel() * x.element_size() for x in (h_c, h_k, h_ql, h_qr))
+    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+    return {"value": us, "unit": "us/layer", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+            "note": "eager calls through the Python binding of the C ABI, one layer cache"}
+
+
+def cpu_baseline(w):
+    n_seq = max(1, w.batch // 16)
+    step, scale = oracle_step_sample(w, n_seq)
+    step()
+    times = [step() for _ in range(3)]
+    us = statistics.mean(times) * scale * 1e6
+    return {"value": us, "unit": "us/layer", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"oracle write of 1 token + decode for {n_seq} of {w.batch} sequences, 3 steps, "
+                      f"scaled x{scale:g} to the full batch"}
+
+
+def main():
+    args = parse()
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_native(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,14 @@
+"""GB300-native (sm_103a) low-bit dual-path MLA KV cache: fused writer and decode attention.
+
+The compute path is the CUDA library libmla_qcache.so (C ABI in include/mla_qcache.h);
+``binding`` marshals torch tensors into it and ``cache.QuantizedMLACache`` owns the device
+buffers (pool, BF16 sink/recent buffers, workspace) of one layer.
+"""
+from .binding import (DEV_BAD_PAGE, DEV_NONFINITE, DEV_RANGE, DEV_ROWS, DEV_SEQ_OVERFLOW, DEV_TIMEOUT, EXPORTS,
+                      Config, QCacheError, lib, make_config, mla_qcache_decode_attn, mla_qcache_write, page_bytes,
+                      strerror, workspace_bytes)
+from .cache import QuantizedMLACache
+
+__all__ = ["Config", "QCacheError", "QuantizedMLACache", "lib", "make_config", "mla_qcache_decode_attn",
+           "mla_qcache_write", "page_bytes", "strerror", "workspace_bytes", "EXPORTS", "DEV_BAD_PAGE",
+           "DEV_NONFINITE", "DEV_RANGE", "DEV_ROWS", "DEV_SEQ_OVERFLOW", "DEV_TIMEOUT"]

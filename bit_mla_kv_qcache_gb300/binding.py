@@ -1,0 +1,138 @@
+"""ctypes binding of the C ABI in include/mla_qcache.h (argument marshalling only).
+
+Every step of the hot path runs in the CUDA kernels of libmla_qcache.so; this module only
+checks tensor dtypes/devices and passes raw pointers, sizes and the current CUDA stream.
+There is no fallback: if the library is missing the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla_qcache.so")
+
+OK, ERR_NULL, ERR_CONFIG, ERR_SHAPE, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA = 0, -1, -2, -3, -4, -5, -6
+DEV_BAD_PAGE, DEV_SEQ_OVERFLOW, DEV_NONFINITE, DEV_RANGE, DEV_ROWS, DEV_TIMEOUT = 1, 2, 4, 8, 16, 32
+
+# the entry points declared in include/mla_qcache.h
+EXPORTS = ("mla_qcache_page_bytes", "mla_qcache_config_check", "mla_qcache_workspace_bytes",
+           "mla_qcache_write", "mla_qcache_decode_attn", "mla_qcache_strerror")
+
+
+class Config(ctypes.Structure):
+    """mla_qcache_config."""
+    _fields_ = [("bits_c", ctypes.c_int32), ("bits_r", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("n_sink", ctypes.c_int32), ("n_recent", ctypes.c_int32), ("clip_q", ctypes.c_float)]
+
+    def __repr__(self):
+        return (f"Config(bits_c={self.bits_c}, bits_r={self.bits_r}, page_size={self.page_size}, "
+                f"n_sink={self.n_sink}, n_recent={self.n_recent}, clip_q={self.clip_q:g})")
+
+
+def make_config(bits_c=4, page_size=128, n_sink=4, n_recent=128, clip_q=None, bits_r=4) -> Config:
+    """C4R4 / C2R4 configuration; the latent clip defaults to 0.94 for INT2 and off for INT4."""
+    if clip_q is None:
+        clip_q = 0.94 if bits_c == 2 else 0.0
+    return Config(bits_c, bits_r, page_size, n_sink, n_recent, clip_q)
+
+
+class QCacheError(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise QCacheError(f"{_LIB_PATH} is not built (run __graft_entry__.build() or "
+                              "python -m bit_mla_kv_qcache_gb300.build)")
+        L = ctypes.CDLL(_LIB_PATH)
+        P, vp, i32, i64, sz = ctypes.POINTER, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        L.mla_qcache_page_bytes.restype = sz
+        L.mla_qcache_page_bytes.argtypes = [P(Config)]
+        L.mla_qcache_config_check.restype = ctypes.c_int
+        L.mla_qcache_config_check.argtypes = [P(Config)]
+        L.mla_qcache_workspace_bytes.restype = sz
+        L.mla_qcache_workspace_bytes.argtypes = [P(Config), i32, i32, i32]
+        L.mla_qcache_write.restype = ctypes.c_int
+        L.mla_qcache_write.argtypes = [P(Config), i32, i32, vp, vp, vp, vp, i32, vp, i32, vp, i64, vp, vp, vp, vp]
+        L.mla_qcache_decode_attn.restype = ctypes.c_int
+        L.mla_qcache_decode_attn.argtypes = [P(Config), i32, i32, vp, vp, vp, i32, vp, vp, i64, vp, vp,
+                                             ctypes.c_float, vp, vp, vp, sz, vp, vp]
+        L.mla_qcache_strerror.restype = ctypes.c_char_p
+        L.mla_qcache_strerror.argtypes = [i32]
+        _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().mla_qcache_strerror(int(status)).decode()
+
+
+def _raise(status: int, what: str):
+    if status != OK:
+        raise QCacheError(f"{what}: {strerror(status)} (status {status})")
+
+
+def page_bytes(cfg: Config) -> int:
+    return int(lib().mla_qcache_page_bytes(ctypes.byref(cfg)))
+
+
+def workspace_bytes(cfg: Config, B: int, H: int, max_pages: int) -> int:
+    return int(lib().mla_qcache_workspace_bytes(ctypes.byref(cfg), B, H, max_pages))
+
+
+def _ptr(t, name, elem_size=None, dtype=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise QCacheError(f"{name} is required")
+    if not t.is_cuda:
+        raise QCacheError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise QCacheError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise QCacheError(f"{name} must be {dtype}, got {t.dtype}")
+    if elem_size is not None and t.element_size() != elem_size:
+        raise QCacheError(f"{name} must have {elem_size}-byte elements")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def mla_qcache_write(cfg: Config, c_new, kr_new, cu_new, seq_lens, max_new: int, page_table, pool,
+                     sink_buf, recent_buf, err_word, stream=None) -> None:
+    """Fused cache writer (see include/mla_qcache.h). BF16 inputs may be bfloat16 or 16-bit ints."""
+    B = seq_lens.shape[0]
+    n_rows = c_new.shape[0]
+    st = lib().mla_qcache_write(
+        ctypes.byref(cfg), B, n_rows, _ptr(c_new, "c_new", 2), _ptr(kr_new, "kr_new", 2),
+        _ptr(cu_new, "cu_new", dtype=torch.int32), _ptr(seq_lens, "seq_lens", dtype=torch.int32), int(max_new),
+        _ptr(page_table, "page_table", dtype=torch.int32), page_table.shape[1], _ptr(pool, "pool", 1),
+        pool.shape[0], _ptr(sink_buf, "sink_buf", 2, allow_none=True) if cfg.n_sink else None,
+        _ptr(recent_buf, "recent_buf", 2), _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
+    _raise(st, "mla_qcache_write")
+
+
+def mla_qcache_decode_attn(cfg: Config, q_lat, q_rope, page_table, seq_lens, pool, sink_buf, recent_buf,
+                           softmax_scale: float, out, lse, workspace, err_word, stream=None) -> None:
+    """Decode attention over the quantized cache (see include/mla_qcache.h)."""
+    B, H = q_lat.shape[0], q_lat.shape[1]
+    st = lib().mla_qcache_decode_attn(
+        ctypes.byref(cfg), B, H, _ptr(q_lat, "q_lat", 2), _ptr(q_rope, "q_rope", 2),
+        _ptr(page_table, "page_table", dtype=torch.int32), page_table.shape[1],
+        _ptr(seq_lens, "seq_lens", dtype=torch.int32), _ptr(pool, "pool", 1), pool.shape[0],
+        _ptr(sink_buf, "sink_buf", 2, allow_none=True) if cfg.n_sink else None, _ptr(recent_buf, "recent_buf", 2),
+        ctypes.c_float(softmax_scale), _ptr(out, "out", dtype=torch.float32), _ptr(lse, "lse", dtype=torch.float32),
+        _ptr(workspace, "workspace", 1), workspace.numel() * workspace.element_size(),
+        _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
+    _raise(st, "mla_qcache_decode_attn")

@@ -1,0 +1,187 @@
+// C ABI entry points (declared in include/mla_qcache.h): host-side validation, problem
+// decomposition and kernel launches on the caller's stream. No allocation, no synchronization.
+#include <cmath>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "kernels.cuh"
+#include "mla_qcache.h"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_config(const mla_qcache_config* c) {
+  if (!c) return MLA_QCACHE_ERR_NULL;
+  if (c->bits_c != 2 && c->bits_c != 4) return MLA_QCACHE_ERR_CONFIG;
+  if (c->bits_r != 4) return MLA_QCACHE_ERR_CONFIG;
+  const int P = c->page_size;
+  if (P != 16 && P != 32 && P != 64 && P != 128) return MLA_QCACHE_ERR_CONFIG;
+  if (c->n_sink < 0 || c->n_sink > 16) return MLA_QCACHE_ERR_CONFIG;
+  if (c->n_recent < P || c->n_recent > 1024) return MLA_QCACHE_ERR_CONFIG;
+  if (!(c->clip_q >= 0.0f && c->clip_q <= 1.0f)) return MLA_QCACHE_ERR_CONFIG;
+  return MLA_QCACHE_OK;
+}
+
+int64_t page_bytes_of(const mla_qcache_config* c) {
+  return static_cast<int64_t>(c->page_size) * (64 * c->bits_c + 48) + 256;
+}
+
+int current_sm_count(int* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_QCACHE_ERR_CUDA;
+  if (cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_QCACHE_ERR_CUDA;
+  return MLA_QCACHE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_qcache_config_check(const mla_qcache_config* cfg) { return check_config(cfg); }
+
+size_t mla_qcache_page_bytes(const mla_qcache_config* cfg) {
+  if (check_config(cfg) != MLA_QCACHE_OK) return 0;
+  return static_cast<size_t>(page_bytes_of(cfg));
+}
+
+size_t mla_qcache_workspace_bytes(const mla_qcache_config* cfg, int32_t B, int32_t H, int32_t max_pages) {
+  if (check_config(cfg) != MLA_QCACHE_OK || B < 1 || H < 16 || H > 256 || H % 16 || max_pages < 1) return 0;
+  int sms = 0;
+  if (current_sm_count(&sms) != MLA_QCACHE_OK) return 0;
+  const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, sms);
+  return mlaq::decode_workspace_bytes(B, H, ns);
+}
+
+int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, const uint16_t* c_new,
+                     const uint16_t* kr_new, const int32_t* cu_new, const int32_t* seq_lens, int32_t max_new,
+                     const int32_t* page_table, int32_t max_pages, uint8_t* pool, int64_t n_pages,
+                     uint16_t* sink_buf, uint16_t* recent_buf, int32_t* err_word, void* stream) {
+  int st = check_config(cfg);
+  if (st != MLA_QCACHE_OK) return st;
+  if (B < 1 || B > (1 << 20) || n_rows < 0 || max_pages < 1 || n_pages < 1) return MLA_QCACHE_ERR_SHAPE;
+  if (n_rows == 0) return MLA_QCACHE_OK;
+  if (max_new < 1) return MLA_QCACHE_ERR_SHAPE;
+  if (!c_new || !kr_new || !cu_new || !seq_lens || !page_table || !pool || !recent_buf || !err_word)
+    return MLA_QCACHE_ERR_NULL;
+  if (cfg->n_sink > 0 && !sink_buf) return MLA_QCACHE_ERR_NULL;
+  if (!aligned(c_new, 16) || !aligned(kr_new, 4) || !aligned(pool, 16) || !aligned(recent_buf, 16) ||
+      (sink_buf && !aligned(sink_buf, 16)) || !aligned(cu_new, 4) || !aligned(seq_lens, 4) ||
+      !aligned(page_table, 4) || !aligned(err_word, 4))
+    return MLA_QCACHE_ERR_ALIGN;
+
+  mlaq::WriteParams p{};
+  p.B = B;
+  p.n_rows = n_rows;
+  p.max_new = max_new;
+  p.max_pages = max_pages;
+  p.P = cfg->page_size;
+  p.S = cfg->n_sink;
+  p.W = cfg->n_recent;
+  p.bits_c = cfg->bits_c;
+  p.clip_k = 0;
+  if (cfg->clip_q > 0.0f) {
+    int k = static_cast<int>(std::ceil(static_cast<double>(cfg->clip_q) * 512.0));
+    p.clip_k = k < 1 ? 1 : (k > 512 ? 512 : k);
+  }
+  p.n_pages = n_pages;
+  p.page_bytes = page_bytes_of(cfg);
+  p.c_new = c_new;
+  p.kr_new = kr_new;
+  p.cu_new = cu_new;
+  p.seq_lens = seq_lens;
+  p.page_table = page_table;
+  p.pool = pool;
+  p.sink = sink_buf;
+  p.ring = recent_buf;
+  p.err = err_word;
+  const int token_blocks = (n_rows + 3) / 4;
+  const int fill_per_seq = max_new / p.P + 1;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (max_new <= p.W - p.P + 1) {
+    // No new token can overwrite a ring row that a page fill of this call still reads.
+    p.token_blocks = token_blocks;
+    p.fill_per_seq = fill_per_seq;
+    e = mlaq::launch_write(p, s);
+  } else {
+    // Page fills first (they read earlier tokens from the ring), then the per-token work.
+    p.token_blocks = 0;
+    p.fill_per_seq = fill_per_seq;
+    e = mlaq::launch_write(p, s);
+    if (e == cudaSuccess) {
+      p.token_blocks = token_blocks;
+      p.fill_per_seq = 0;
+      e = mlaq::launch_write(p, s);
+    }
+  }
+  return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
+}
+
+int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H, const uint16_t* q_lat,
+                           const uint16_t* q_rope, const int32_t* page_table, int32_t max_pages,
+                           const int32_t* seq_lens, const uint8_t* pool, int64_t n_pages,
+                           const uint16_t* sink_buf, const uint16_t* recent_buf, float softmax_scale, float* out,
+                           float* lse, void* workspace, size_t workspace_bytes, int32_t* err_word, void* stream) {
+  int st = check_config(cfg);
+  if (st != MLA_QCACHE_OK) return st;
+  if (B < 1 || B > 65535 || H < 16 || H > 256 || H % 16 || max_pages < 1 || n_pages < 1)
+    return MLA_QCACHE_ERR_SHAPE;
+  if (!q_lat || !q_rope || !page_table || !seq_lens || !pool || !recent_buf || !out || !lse || !workspace ||
+      !err_word)
+    return MLA_QCACHE_ERR_NULL;
+  if (cfg->n_sink > 0 && !sink_buf) return MLA_QCACHE_ERR_NULL;
+  if (!aligned(q_lat, 4) || !aligned(q_rope, 4) || !aligned(pool, 16) || !aligned(recent_buf, 16) ||
+      (sink_buf && !aligned(sink_buf, 16)) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(workspace, 16) ||
+      !aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(err_word, 4))
+    return MLA_QCACHE_ERR_ALIGN;
+  int sms = 0;
+  st = current_sm_count(&sms);
+  if (st != MLA_QCACHE_OK) return st;
+  const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, sms);
+  const size_t need = mlaq::decode_workspace_bytes(B, H, ns);
+  if (workspace_bytes < need) return MLA_QCACHE_ERR_WORKSPACE;
+
+  mlaq::DecodeParams p{};
+  p.q_lat = q_lat;
+  p.q_rope = q_rope;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.pool = pool;
+  p.sink = sink_buf;
+  p.ring = recent_buf;
+  p.o_part = static_cast<float*>(workspace);
+  p.ml_part = static_cast<float*>(workspace) + static_cast<size_t>(B) * H * (ns + 1) * mlaq::kLatent;
+  p.out = out;
+  p.lse = lse;
+  p.err = err_word;
+  p.n_pages = n_pages;
+  p.page_bytes = page_bytes_of(cfg);
+  p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634074);
+  p.B = B;
+  p.H = H;
+  p.max_pages = max_pages;
+  p.P = cfg->page_size;
+  p.S = cfg->n_sink;
+  p.W = cfg->n_recent;
+  p.bits_c = cfg->bits_c;
+  p.n_split = ns;
+  const cudaError_t e = mlaq::launch_decode(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
+}
+
+const char* mla_qcache_strerror(int32_t status) {
+  switch (status) {
+    case MLA_QCACHE_OK: return "ok";
+    case MLA_QCACHE_ERR_NULL: return "a required pointer is NULL";
+    case MLA_QCACHE_ERR_CONFIG: return "unsupported cache configuration";
+    case MLA_QCACHE_ERR_SHAPE: return "invalid size argument (B, H, rows, pages or max_new)";
+    case MLA_QCACHE_ERR_ALIGN: return "pointer not aligned as documented";
+    case MLA_QCACHE_ERR_WORKSPACE: return "workspace too small";
+    case MLA_QCACHE_ERR_CUDA: return "CUDA runtime error while launching";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

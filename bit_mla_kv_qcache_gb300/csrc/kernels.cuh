@@ -1,0 +1,69 @@
+// Kernel parameter blocks and launchers shared by the C ABI layer (abi.cu) and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace mlaq {
+
+constexpr int kLatent = 512;
+constexpr int kRope = 64;
+constexpr int kRow = 576;
+constexpr int kGroup = 128;
+
+// Device error bits (same values as MLA_QCACHE_DEV_* in the public header).
+constexpr int kErrBadPage = 1;
+constexpr int kErrSeqOverflow = 2;
+constexpr int kErrNonFinite = 4;
+constexpr int kErrRange = 8;
+constexpr int kErrRows = 16;
+constexpr int kErrTimeout = 32;
+
+struct WriteParams {
+  int B, n_rows, max_new, max_pages;
+  int P, S, W, bits_c, clip_k;  // clip_k: rank of the clip order statistic (0 = no clip)
+  int64_t n_pages;
+  int64_t page_bytes;
+  const uint16_t* c_new;
+  const uint16_t* kr_new;
+  const int32_t* cu_new;
+  const int32_t* seq_lens;
+  const int32_t* page_table;
+  uint8_t* pool;
+  uint16_t* sink;
+  uint16_t* ring;
+  int32_t* err;
+  int token_blocks;  // blocks [0, token_blocks) do per-token work (4 tokens per block)
+  int fill_per_seq;  // page-fill blocks per sequence after the token blocks
+};
+
+// One launch doing per-token packing/retention (token_blocks > 0) and/or page fills.
+cudaError_t launch_write(const WriteParams& p, cudaStream_t stream);
+
+struct DecodeParams {
+  const uint16_t* q_lat;
+  const uint16_t* q_rope;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const uint8_t* pool;
+  const uint16_t* sink;
+  const uint16_t* ring;
+  float* o_part;  // [B][H][NS][512] partial (unnormalized) outputs
+  float* ml_part; // [B][H][NS][2] partial (max in log2 units, sum)
+  float* out;     // [B][H][512]
+  float* lse;     // [B][H]
+  int32_t* err;
+  int64_t n_pages;
+  int64_t page_bytes;
+  float scale_log2;  // softmax_scale * log2(e)
+  int B, H, max_pages, P, S, W, bits_c;
+  int n_split;  // splits of the packed tokens; split index n_split is the BF16 (protected) split
+};
+
+// Number of packed-token splits for a problem size (depends on the SM count).
+int decode_num_splits(int B, int H, int max_pages, int P, int num_sms);
+size_t decode_workspace_bytes(int B, int H, int n_split);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+
+}  // namespace mlaq

@@ -1,0 +1,93 @@
+"""The C ABI library loads and exports every entry point include/mla_qcache.h declares; host-side
+validation answers without touching a GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from bit_mla_kv_qcache_gb300 import build
+    build.build()
+    import bit_mla_kv_qcache_gb300 as q
+    return q
+
+
+def _declared():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", h)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names += re.findall(r"\b(mla_qcache_\w+)\s*\(", txt)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(L):
+    declared = _declared()
+    assert len(declared) >= 6
+    lib = L.lib()
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(L.EXPORTS) <= set(declared)
+
+
+def test_page_bytes_and_config_check(L):
+    assert L.page_bytes(L.make_config(4, 128)) == 39168
+    assert L.page_bytes(L.make_config(2, 64)) == 11520
+    lib = L.lib()
+    bad = [L.make_config(3, 128), L.make_config(4, 96), L.make_config(4, 128, n_recent=64),
+           L.make_config(4, 64, n_sink=17), L.make_config(4, 64, clip_q=1.5), L.make_config(4, 64, bits_r=2)]
+    for c in bad:
+        assert lib.mla_qcache_config_check(ctypes.byref(c)) == -2
+        assert L.page_bytes(c) == 0
+    assert lib.mla_qcache_config_check(None) == -1
+    assert lib.mla_qcache_config_check(ctypes.byref(L.make_config(2, 64))) == 0
+
+
+def test_strerror(L):
+    for s in range(-6, 1):
+        assert isinstance(L.strerror(s), str) and L.strerror(s)
+    assert L.strerror(-99) == "unknown status"
+
+
+def test_host_validation_without_gpu(L):
+    lib = L.lib()
+    cfg = L.make_config(4, 128)
+    p = ctypes.c_void_p(16 * 1024)  # never dereferenced: validation fails first
+    # zero rows: nothing to do
+    assert lib.mla_qcache_write(ctypes.byref(cfg), 1, 0, None, None, None, None, 1, None, 1, None, 1, None, None,
+                                None, None) == 0
+    # missing pointers
+    assert lib.mla_qcache_write(ctypes.byref(cfg), 1, 4, None, p, p, p, 1, p, 1, p, 1, p, p, p, None) == -1
+    # bad sizes
+    assert lib.mla_qcache_write(ctypes.byref(cfg), 0, 4, p, p, p, p, 1, p, 1, p, 1, p, p, p, None) == -3
+    assert lib.mla_qcache_write(ctypes.byref(cfg), 1, 4, p, p, p, p, 0, p, 1, p, 1, p, p, p, None) == -3
+    # misaligned pool
+    assert lib.mla_qcache_write(ctypes.byref(cfg), 1, 4, p, p, p, p, 1, p, 1, ctypes.c_void_p(16 * 1024 + 4), 1,
+                                p, p, p, None) == -4
+    f = ctypes.c_float(0.1)
+    # decode: H not a multiple of 16, null output, bad config
+    assert lib.mla_qcache_decode_attn(ctypes.byref(cfg), 1, 24, p, p, p, 1, p, p, 1, p, p, f, p, p, p, 1 << 20, p,
+                                      None) == -3
+    assert lib.mla_qcache_decode_attn(ctypes.byref(cfg), 1, 16, p, p, p, 1, p, p, 1, p, p, f, None, p, p, 1 << 20,
+                                      p, None) == -1
+    bad = L.make_config(4, 128, n_recent=64)
+    assert lib.mla_qcache_decode_attn(ctypes.byref(bad), 1, 16, p, p, p, 1, p, p, 1, p, p, f, p, p, p, 1 << 20, p,
+                                      None) == -2
+
+
+def test_product_path_has_no_cpu_fallback(L, monkeypatch):
+    """Without the built library the binding raises instead of computing anything else."""
+    import bit_mla_kv_qcache_gb300.binding as b
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "_LIB_PATH", "/nonexistent/libmla_qcache.so")
+    with pytest.raises(b.QCacheError):
+        b.lib()
+    src = open(os.path.join(ROOT, "bit_mla_kv_qcache_gb300", "binding.py")).read()
+    src += open(os.path.join(ROOT, "bit_mla_kv_qcache_gb300", "cache.py")).read()
+    assert "import oracle" not in src and "from oracle" not in src

@@ -1,0 +1,101 @@
+"""Decode-attention parity on the GPU against the fp64 oracle.
+
+Tolerance (stated for the method's output): per (sequence, head) row, max |O - O*| / max |O*|
+<= 2e-3, and |LSE - LSE*| <= 2e-3 (fp32 accumulation against fp64).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+def _run(w, lens, heads=None, extra_pages=0, scale=None):
+    inp = workloads.make_inputs(w, seq_lens=np.array(lens, np.int32), extra_pages=extra_pages, heads=heads)
+    kw = w.config_kwargs()
+    cache = gu.gpu_cache(kw, inp)
+    if inp.c.shape[0]:
+        gu.write_rows(cache, inp.c, inp.kr, inp.seq_lens, max(1, int(inp.seq_lens.max())))
+    sc = w.softmax_scale if scale is None else scale
+    out, lse = cache.decode(gu.dev(inp.q_lat), gu.dev(inp.q_rope), sc)
+    torch.cuda.synchronize()
+    assert cache.error_bits() == 0, cache.error_bits()
+    cfg, pool, sink, ring = gu.oracle_cache(kw, inp)
+    if inp.c.shape[0]:
+        assert oracle.write(cfg, inp.c, inp.kr, inp.cu, np.zeros(len(lens), np.int32),
+                            max(1, int(inp.seq_lens.max())), inp.page_table, pool, sink, ring) == 0
+    gu.assert_cache_equal(cache, pool, sink, ring)
+    o_ref, l_ref, fl = oracle.decode(cfg, inp.q_lat, inp.q_rope, inp.page_table, inp.seq_lens, pool, sink, ring, sc)
+    assert fl == 0
+    return gu.check_decode(out, lse, o_ref, l_ref, TOL)
+
+
+C4 = workloads.Workload("c4", 1, 16, 1, 4, 128, random_pages=True, seed=21)
+C2 = workloads.Workload("c2", 1, 16, 1, 2, 64, clip_q=0.94, latent_dist="student_t5", n_outliers=8,
+                        outlier_scale=20.0, random_pages=True, seed=22)
+
+
+@pytest.mark.parametrize("T", [0, 1, 2, 4, 5, 131, 132, 133, 127, 128, 129, 259, 1000])
+def test_boundaries_c4(T):
+    _run(C4, [T, max(0, T - 1)])
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 131, 132, 133, 195, 777])
+def test_boundaries_c2(T):
+    _run(C2, [T, T + 16, 3])
+
+
+def test_tiny_workload_full():
+    w = workloads.WORKLOADS["tiny_c4r4_b1_h16_t1k"]
+    _run(w, [w.seq_len])
+
+
+@pytest.mark.parametrize("heads", [32, 128])
+def test_more_heads(heads):
+    _run(C4, [700, 300], heads=heads)
+
+
+def test_no_sink_small_window_small_pages():
+    w = workloads.Workload("s0", 1, 16, 1, 4, 16, n_sink=0, n_recent=16, random_pages=True, seed=5)
+    _run(w, [500, 17, 16, 15])
+
+
+def test_wide_window_and_sinks():
+    w = workloads.Workload("s16", 1, 16, 1, 2, 32, n_sink=16, n_recent=256, clip_q=0.94, random_pages=True, seed=6)
+    _run(w, [900, 272, 271, 40])
+
+
+def test_ragged_batch_c2r4_serving_shape():
+    w = workloads.WORKLOADS["ragged_c2r4_b64_h16_serve"]
+    rng = np.random.default_rng(77)
+    lens = rng.integers(1, 1500, size=64)
+    _run(w, lens)
+
+
+def test_peaked_softmax():
+    """A large softmax scale concentrates the weights (stresses the running-max rescaling)."""
+    _run(C4, [600, 250], scale=0.5)
+
+
+def test_full_size_v2lite_decode():
+    """The 32 x 8192-token C4R4 decode in the configuration the benchmark times."""
+    w = workloads.WORKLOADS["v2lite_c4r4_b32_h16_t8k"]
+    rel, dl = _run(w, [w.seq_len] * w.batch, extra_pages=1)
+    print(f"full-size rel {rel:.2e} dlse {dl:.2e}")
+
+
+def test_bad_page_sets_error_bit():
+    inp = workloads.make_inputs(C4, seq_lens=np.array([700], np.int32))
+    kw = C4.config_kwargs()
+    cache = gu.gpu_cache(kw, inp)
+    gu.write_rows(cache, inp.c, inp.kr, inp.seq_lens, 700)
+    cache.page_table[0, 2] = 10 ** 6
+    out, lse = cache.decode(gu.dev(inp.q_lat), gu.dev(inp.q_rope), C4.softmax_scale)
+    torch.cuda.synchronize()
+    assert cache.error_bits() & 1
+    assert torch.isfinite(out).all()

@@ -15,7 +15,8 @@ import oracle
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 # every finite FP16 value as an exact rational, sorted
-_F16 = np.arange(65536, dtype=np.uint16).view(np.float16).astype(np.float64)
+with np.errstate(invalid="ignore"):
+    _F16 = np.arange(65536, dtype=np.uint16).view(np.float16).astype(np.float64)
 _F16_FINITE = sorted({Fraction(float(v)) for v in _F16 if np.isfinite(v)})
 
 
