@@ -14,11 +14,13 @@ import torch
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla_qcache.so")
 
 OK, ERR_NULL, ERR_CONFIG, ERR_SHAPE, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA = 0, -1, -2, -3, -4, -5, -6
+ERR_SCRATCH_LIMIT = -7
 DEV_BAD_PAGE, DEV_SEQ_OVERFLOW, DEV_NONFINITE, DEV_RANGE, DEV_ROWS, DEV_TIMEOUT = 1, 2, 4, 8, 16, 32
 
 # the entry points declared in include/mla_qcache.h
 EXPORTS = ("mla_qcache_page_bytes", "mla_qcache_config_check", "mla_qcache_workspace_bytes",
-           "mla_qcache_write", "mla_qcache_decode_attn", "mla_qcache_strerror")
+           "mla_qcache_write", "mla_qcache_decode_attn", "mla_qcache_strerror",
+           "mla_qcache_decode_attn_noalloc", "mla_qcache_noalloc_scratch_bytes")
 
 
 class Config(ctypes.Structure):
@@ -64,6 +66,11 @@ def lib() -> ctypes.CDLL:
         L.mla_qcache_decode_attn.restype = ctypes.c_int
         L.mla_qcache_decode_attn.argtypes = [P(Config), i32, i32, vp, vp, vp, i32, vp, vp, i64, vp, vp,
                                              ctypes.c_float, vp, vp, vp, sz, vp, vp]
+        L.mla_qcache_decode_attn_noalloc.restype = ctypes.c_int
+        L.mla_qcache_decode_attn_noalloc.argtypes = [P(Config), i32, i32, vp, vp, vp, i32, vp, vp, i64, vp, vp,
+                                                     ctypes.c_float, vp, vp, vp, vp]
+        L.mla_qcache_noalloc_scratch_bytes.restype = sz
+        L.mla_qcache_noalloc_scratch_bytes.argtypes = []
         L.mla_qcache_strerror.restype = ctypes.c_char_p
         L.mla_qcache_strerror.argtypes = [i32]
         _lib = L
@@ -136,3 +143,23 @@ def mla_qcache_decode_attn(cfg: Config, q_lat, q_rope, page_table, seq_lens, poo
         _ptr(workspace, "workspace", 1), workspace.numel() * workspace.element_size(),
         _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
     _raise(st, "mla_qcache_decode_attn")
+
+
+def noalloc_scratch_bytes() -> int:
+    """Size of the scratch built into the library for mla_qcache_decode_attn_noalloc."""
+    return int(lib().mla_qcache_noalloc_scratch_bytes())
+
+
+def mla_qcache_decode_attn_noalloc(cfg: Config, q_lat, q_rope, page_table, seq_lens, pool, sink_buf, recent_buf,
+                                   softmax_scale: float, out, lse, err_word, stream=None) -> None:
+    """Decode attention without a workspace argument: for callers that cannot allocate device
+    memory, it runs on a scratch buffer compiled into the library (see include/mla_qcache.h)."""
+    B, H = q_lat.shape[0], q_lat.shape[1]
+    st = lib().mla_qcache_decode_attn_noalloc(
+        ctypes.byref(cfg), B, H, _ptr(q_lat, "q_lat", 2), _ptr(q_rope, "q_rope", 2),
+        _ptr(page_table, "page_table", dtype=torch.int32), page_table.shape[1],
+        _ptr(seq_lens, "seq_lens", dtype=torch.int32), _ptr(pool, "pool", 1), pool.shape[0],
+        _ptr(sink_buf, "sink_buf", 2, allow_none=True) if cfg.n_sink else None, _ptr(recent_buf, "recent_buf", 2),
+        ctypes.c_float(softmax_scale), _ptr(out, "out", dtype=torch.float32), _ptr(lse, "lse", dtype=torch.float32),
+        _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
+    _raise(st, "mla_qcache_decode_attn_noalloc")

@@ -171,6 +171,29 @@ int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H, c
   return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
 }
 
+int mla_qcache_decode_attn_noalloc(const mla_qcache_config* cfg, int32_t B, int32_t H, const uint16_t* q_lat,
+                                   const uint16_t* q_rope, const int32_t* page_table, int32_t max_pages,
+                                   const int32_t* seq_lens, const uint8_t* pool, int64_t n_pages,
+                                   const uint16_t* sink_buf, const uint16_t* recent_buf, float softmax_scale,
+                                   float* out, float* lse, int32_t* err_word, void* stream) {
+  int st = check_config(cfg);
+  if (st != MLA_QCACHE_OK) return st;
+  if (B < 1 || B > 65535 || H < 16 || H > 256 || H % 16 || max_pages < 1 || n_pages < 1)
+    return MLA_QCACHE_ERR_SHAPE;
+  int sms = 0;
+  st = current_sm_count(&sms);
+  if (st != MLA_QCACHE_OK) return st;
+  const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, sms);
+  if (mlaq::decode_workspace_bytes(B, H, ns) > mlaq::kNoAllocScratchBytes) return MLA_QCACHE_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  if (mlaq::noalloc_scratch(&scratch) != cudaSuccess) return MLA_QCACHE_ERR_CUDA;
+  return mla_qcache_decode_attn(cfg, B, H, q_lat, q_rope, page_table, max_pages, seq_lens, pool, n_pages, sink_buf,
+                                recent_buf, softmax_scale, out, lse, scratch, mlaq::kNoAllocScratchBytes, err_word,
+                                stream);
+}
+
+size_t mla_qcache_noalloc_scratch_bytes(void) { return mlaq::kNoAllocScratchBytes; }
+
 const char* mla_qcache_strerror(int32_t status) {
   switch (status) {
     case MLA_QCACHE_OK: return "ok";
@@ -180,6 +203,8 @@ const char* mla_qcache_strerror(int32_t status) {
     case MLA_QCACHE_ERR_ALIGN: return "pointer not aligned as documented";
     case MLA_QCACHE_ERR_WORKSPACE: return "workspace too small";
     case MLA_QCACHE_ERR_CUDA: return "CUDA runtime error while launching";
+    case MLA_QCACHE_ERR_SCRATCH_LIMIT:
+      return "problem needs more scratch than the built-in buffer of mla_qcache_decode_attn_noalloc holds";
     default: return "unknown status";
   }
 }

@@ -631,24 +631,60 @@ size_t decode_workspace_bytes(int B, int H, int n_split) {
   return static_cast<size_t>(B) * H * NS * (kLatent + 2) * sizeof(float);
 }
 
+// The dynamic shared-memory opt-in is a per-device function attribute: set it once per device
+// (never inside a stream capture after the first call).
+template <int BITS>
+cudaError_t ensure_smem_attr() {
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!done[dev]) {
+    e = cudaFuncSetAttribute(decode_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(BITS));
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   const dim3 grid(p.n_split + 1, p.H / 16, p.B);
   cudaError_t e;
   if (p.bits_c == 4) {
-    const int smem = smem_bytes(4);
-    e = cudaFuncSetAttribute(decode_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    decode_kernel<4><<<grid, kThreads, smem, stream>>>(p);
+    if ((e = ensure_smem_attr<4>()) != cudaSuccess) return e;
+    decode_kernel<4><<<grid, kThreads, smem_bytes(4), stream>>>(p);
   } else {
-    const int smem = smem_bytes(2);
-    e = cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    decode_kernel<2><<<grid, kThreads, smem, stream>>>(p);
+    if ((e = ensure_smem_attr<2>()) != cudaSuccess) return e;
+    decode_kernel<2><<<grid, kThreads, smem_bytes(2), stream>>>(p);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   combine_kernel<<<p.B * p.H, 128, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ built-in scratch
+// Device-resident scratch used by mla_qcache_decode_attn_noalloc in place of a caller workspace.
+// It lives for as long as the library is loaded, on every device that loads it.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch for the current device. The host-side name of the array is only
+// a stand-in, so the address is looked up once per device (with that device current) and cached.
+cudaError_t noalloc_scratch(void** out) {
+  static void* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace mlaq

@@ -66,4 +66,8 @@ int decode_num_splits(int B, int H, int max_pages, int P, int num_sms);
 size_t decode_workspace_bytes(int B, int H, int n_split);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 
+// Built-in decode scratch for callers that cannot allocate (mla_qcache_decode_attn_noalloc).
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+cudaError_t noalloc_scratch(void** out);
+
 }  // namespace mlaq

@@ -58,6 +58,7 @@ extern "C" {
 #define MLA_QCACHE_ERR_ALIGN (-4)     /* a pointer is not aligned as documented */
 #define MLA_QCACHE_ERR_WORKSPACE (-5) /* workspace too small */
 #define MLA_QCACHE_ERR_CUDA (-6)      /* a CUDA runtime call failed (launch, attribute, ...) */
+#define MLA_QCACHE_ERR_SCRATCH_LIMIT (-7) /* too large for the built-in scratch (noalloc variant) */
 
 /* Device-side error bits, OR-ed into *err_word. */
 #define MLA_QCACHE_DEV_BAD_PAGE 1      /* page-table entry outside [0, n_pages) */
@@ -216,6 +217,38 @@ int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H,
                            const uint16_t* sink_buf, const uint16_t* recent_buf,
                            float softmax_scale, float* out, float* lse, void* workspace,
                            size_t workspace_bytes, int32_t* err_word, void* stream);
+
+/*
+ * Decode attention that allocates nothing, for callers that cannot call cudaMalloc: for
+ * example a plugin inside a host runtime that owns all device memory through its own
+ * allocator and forbids direct allocations, or a latency-critical serving loop that must
+ * never trigger a device allocation (which can synchronize the device or fail under a memory
+ * budget fixed at startup). There is no counterpart on the pages; it is the same computation
+ * as mla_qcache_decode_attn with the same arguments minus the workspace.
+ *
+ * Instead of a caller workspace it uses a scratch array compiled into this library: a static
+ * device buffer of mla_qcache_noalloc_scratch_bytes() bytes (16 MiB) that every GPU which
+ * loads the library holds until the process exits. Problems whose split partials do not fit
+ * (mla_qcache_workspace_bytes() above that size) are rejected with
+ * MLA_QCACHE_ERR_SCRATCH_LIMIT and nothing is launched. The entry point calls no cudaMalloc,
+ * cudaFree or allocating library routine.
+ *
+ * The first call on a device looks up the scratch's device address (cudaGetSymbolAddress, with
+ * that device current) and caches it; make that first call before any stream capture. Every
+ * call shares the one array and leaves its contents behind; nothing in it needs to start at
+ * zero because each call writes every partial result it later reads. Calls that overlap on the
+ * GPU (two streams, or two host threads) race on the scratch: serialize them.
+ */
+int mla_qcache_decode_attn_noalloc(const mla_qcache_config* cfg, int32_t B, int32_t H,
+                                   const uint16_t* q_lat, const uint16_t* q_rope,
+                                   const int32_t* page_table, int32_t max_pages,
+                                   const int32_t* seq_lens, const uint8_t* pool, int64_t n_pages,
+                                   const uint16_t* sink_buf, const uint16_t* recent_buf,
+                                   float softmax_scale, float* out, float* lse, int32_t* err_word,
+                                   void* stream);
+
+/* Size in bytes of the built-in scratch used by mla_qcache_decode_attn_noalloc. */
+size_t mla_qcache_noalloc_scratch_bytes(void);
 
 /* Static description of a status code (never NULL). */
 const char* mla_qcache_strerror(int32_t status);
