@@ -31,6 +31,8 @@ constexpr int kTile = 16;
 constexpr int kRowStride = 24;              // floats per head row in the score / P exchange
 constexpr int kBf16RowBytes = kRow * 2 + 16;  // padded BF16 row in shared memory (1168 B)
 constexpr long long kWaitBudget = 4ll << 30;  // ~2 s at 2 GHz before a wait gives up
+constexpr float kRescaleSlack = 8.f;          // softmax weights stay <= 2^8 between rescales
+constexpr float kStrictScale = 255.f;         // a token scale >= this forces weights <= 1 (FP16 safety)
 
 __host__ __device__ constexpr int packed_stage_bytes(int bits) { return kTile * 64 * bits + 512 + 256 + 256; }
 __host__ __device__ constexpr int stage_region_bytes(int bits) {
@@ -40,7 +42,7 @@ __host__ __device__ constexpr int stage_region_bytes(int bits) {
 constexpr int kSbufFloats = 2 * 4 * 16 * kRowStride;
 constexpr int kPbufFloats = 2 * 16 * kRowStride;
 __host__ __device__ constexpr int smem_bytes(int bits) {
-  return stage_region_bytes(bits) + (kSbufFloats + kPbufFloats + 2 * 16) * 4 + kStages * 8;
+  return stage_region_bytes(bits) + (kSbufFloats + kPbufFloats + 2 * 16) * 4 + kStages * 8 + 2 * 4;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -65,6 +67,7 @@ struct Shared {
   float* pbuf;   // [2][16 heads][kRowStride]
   float* alpha;  // [2][16]
   uint64_t* bars;
+  int* strict;   // [2] per exchange buffer: a sub-tile needs an exact running max
 };
 
 template <int BITS>
@@ -75,6 +78,7 @@ __device__ __forceinline__ Shared carve(uint8_t* smem) {
   s.pbuf = s.sbuf + kSbufFloats;
   s.alpha = s.pbuf + kPbufFloats;
   s.bars = reinterpret_cast<uint64_t*>(s.alpha + 2 * 16);
+  s.strict = reinterpret_cast<int*>(s.bars + kStages);
   return s;
 }
 
@@ -82,11 +86,19 @@ __device__ __forceinline__ Shared carve(uint8_t* smem) {
 struct State {
   float o[16][4];  // readout accumulators: channel block cb (8 channels), C fragment
   float mterm[2];  // sum_t p_t * min_t for rows g, g+8 (packed path only)
-  float m_run, l_run;  // softmax state of head 4*warp + lane/8 (log2 units)
+  float m_run;     // reference max of head 4*warp + lane/8 (log2 units), shared by its 8 lanes
+  float l_part;    // this lane's share of the running sum (reduced over the 8 lanes at the end)
 };
 
 // Exchange the warps' partial scores, run the online softmax for 4 heads per warp, publish
-// P and the rescale factors. Two CTA barriers; returns true if any thread saw a timeout.
+// P and (when some head's reference max moved) the rescale factors. Two CTA barriers; returns
+// true if any thread saw a timeout. sh.strict[buf] (a CTA-wide flag for this sub-tile) forces
+// an exact running max so that every weight stays <= 1.
+//
+// Lazy rescaling: the reference max of a head moves only when a tile exceeds it by more than
+// kRescaleSlack (log2 units), so the weights stay <= 2^kRescaleSlack, the accumulators are
+// rescaled rarely and the common path needs no cross-lane reduction. The result does not
+// depend on the reference (it cancels in O / l and is accounted for in the LSE).
 __device__ __forceinline__ bool exchange_softmax(const Shared& sh, int buf, const float (&part)[2][4], int t0,
                                                  int lo, int hi, float scale_log2, State& st, bool timed_out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
@@ -97,6 +109,7 @@ __device__ __forceinline__ bool exchange_softmax(const Shared& sh, int buf, cons
     *reinterpret_cast<float2*>(my + (g + 8) * kRowStride + 8 * nb + 2 * q) = make_float2(part[nb][2], part[nb][3]);
   }
   if (__syncthreads_or(timed_out)) return true;
+  const bool strict = sh.strict[buf] != 0;
 
   const int hh = 4 * warp + (lane >> 3), tt = 2 * (lane & 7);
   float s0 = 0.f, s1 = 0.f;
@@ -110,38 +123,44 @@ __device__ __forceinline__ bool exchange_softmax(const Shared& sh, int buf, cons
   const bool v1 = (t0 + tt + 1 >= lo) && (t0 + tt + 1 < hi);
   s0 = v0 ? s0 * scale_log2 : -INFINITY;
   s1 = v1 ? s1 * scale_log2 : -INFINITY;
-  float tmax = fmaxf(s0, s1);
+  const float lmax = fmaxf(s0, s1);
+  const float slack = strict ? 0.f : kRescaleSlack;
+  const bool need = lmax > st.m_run + slack || (st.m_run == -INFINITY && lmax > -INFINITY);
+  float alpha = 1.f;
+  const bool moved = __any_sync(0xffffffffu, need);
+  if (moved) {  // rare: some head of this warp needs a new reference max
+    float tmax = lmax;
 #pragma unroll
-  for (int o = 1; o < 8; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-  const float m_new = fmaxf(st.m_run, tmax);
-  float alpha, p0, p1;
-  if (m_new == -INFINITY) {
-    alpha = 1.f;
-    p0 = p1 = 0.f;
-  } else {
-    alpha = exp2f(st.m_run - m_new);
-    p0 = v0 ? exp2f(s0 - m_new) : 0.f;
-    p1 = v1 ? exp2f(s1 - m_new) : 0.f;
+    for (int o = 1; o < 8; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+    if (tmax > st.m_run + slack || (st.m_run == -INFINITY && tmax > -INFINITY)) {
+      alpha = exp2f(st.m_run - tmax);  // 0 when the old reference was -inf
+      st.l_part *= alpha;
+      st.m_run = tmax;
+    }
   }
-  float psum = p0 + p1;
-#pragma unroll
-  for (int o = 1; o < 8; o <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
-  st.l_run = st.l_run * alpha + psum;
-  st.m_run = m_new;
+  float p0 = 0.f, p1 = 0.f;
+  if (st.m_run != -INFINITY) {
+    p0 = v0 ? exp2f(s0 - st.m_run) : 0.f;
+    p1 = v1 ? exp2f(s1 - st.m_run) : 0.f;
+  }
+  st.l_part += p0 + p1;
   *reinterpret_cast<float2*>(sh.pbuf + (buf * 16 + hh) * kRowStride + tt) = make_float2(p0, p1);
   if ((lane & 7) == 0) sh.alpha[buf * 16 + hh] = alpha;
-  __syncthreads();
+  const bool any_rescale = __syncthreads_or(moved);
+  if (threadIdx.x == 0) sh.strict[buf] = 0;  // consumed; the next use of this buffer sets it afresh
 
-  const float a0 = sh.alpha[buf * 16 + g], a1 = sh.alpha[buf * 16 + g + 8];
+  if (any_rescale) {
+    const float a0 = sh.alpha[buf * 16 + g], a1 = sh.alpha[buf * 16 + g + 8];
 #pragma unroll
-  for (int cb = 0; cb < 16; ++cb) {
-    st.o[cb][0] *= a0;
-    st.o[cb][1] *= a0;
-    st.o[cb][2] *= a1;
-    st.o[cb][3] *= a1;
+    for (int cb = 0; cb < 16; ++cb) {
+      st.o[cb][0] *= a0;
+      st.o[cb][1] *= a0;
+      st.o[cb][2] *= a1;
+      st.o[cb][3] *= a1;
+    }
+    st.mterm[0] *= a0;
+    st.mterm[1] *= a1;
   }
-  st.mterm[0] *= a0;
-  st.mterm[1] *= a1;
   return false;
 }
 
@@ -293,15 +312,25 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
     }
 
     // ---- scores on tensor cores
-    float acc[2][4], racc[2][4];
+    // four independent accumulation chains per n-block pair keep the tensor pipe busy
+    float acc[2][4], acc1[2][4], racc[2][4];
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[nb][e] = acc1[nb][e] = racc[nb][e] = 0.f;
+#pragma unroll
+    for (int kc = 0; kc < 8; kc += 2)
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb) {
+        mma_bf16_16816(acc[nb], qa[kc], bq[nb][kc][0], bq[nb][kc][1]);
+        mma_bf16_16816(acc1[nb], qa[kc + 1], bq[nb][kc + 1][0], bq[nb][kc + 1][1]);
+      }
 #pragma unroll
     for (int nb = 0; nb < 2; ++nb) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[nb][e] = racc[nb][e] = 0.f;
-#pragma unroll
-      for (int kc = 0; kc < 8; ++kc) mma_bf16_16816(acc[nb], qa[kc], bq[nb][kc][0], bq[nb][kc][1]);
       mma_bf16_16816(racc[nb], qr_hi, rb[nb][0], rb[nb][1]);
       mma_bf16_16816(racc[nb], qr_lo, rb[nb][0], rb[nb][1]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[nb][e] += acc1[nb][e];
     }
     // token metadata: group `warp`, tokens 8nb + 2q + e
     float tsc[2][2], tmn[2][2];
@@ -323,8 +352,19 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
         part[nb][e] = tsc[nb][c] * (acc[nb][e] - 128.f * qsum[r]) + tmn[nb][c] * qsum[r] +
                       (racc[nb][e] - 128.f * rqs[r]) + rbias[r];
       }
-
+    // token scales large enough that p * scale could overflow FP16 when p reaches 2^8
     const int buf = i & 1;
+    if (fmaxf(fmaxf(tsc[0][0], tsc[0][1]), fmaxf(tsc[1][0], tsc[1][1])) >= kStrictScale) sh.strict[buf] = 1;
+
+    // transpose the codes into the readout operand while the exchange is in flight:
+    // 0x4300|n read as FP16 is 3.5 + n/512; subtracting 3.5 leaves n/512 exactly
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) bq[nb][kc][r] = hsub2_u32(movmatrix_t(bq[nb][kc][r]), 0x43004300u);
+
     if (exchange_softmax(sh, buf, part, t0, lo, hi, p.scale_log2, st, !ok)) {
       flags |= kErrTimeout;
       // orderly exit: bounded waits for the copies still in flight into this CTA
@@ -353,12 +393,7 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
 #pragma unroll
     for (int kc = 0; kc < 8; ++kc)
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        // 0x4300|n read as FP16 is 3.5 + n/512; subtracting 3.5 leaves n/512 exactly
-        const uint32_t v0 = hsub2_u32(movmatrix_t(bq[0][kc][r]), 0x43004300u);
-        const uint32_t v1 = hsub2_u32(movmatrix_t(bq[1][kc][r]), 0x43004300u);
-        mma_f16_16816(st.o[2 * kc + r], a, v0, v1);
-      }
+      for (int r = 0; r < 2; ++r) mma_f16_16816(st.o[2 * kc + r], a, bq[0][kc][r], bq[1][kc][r]);
   }
 }
 
@@ -488,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) mbar_init(sh.bars + i, 1);
     fence_mbar_init();
+    sh.strict[0] = sh.strict[1] = 0;
   }
   __syncthreads();
 
@@ -537,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
   for (int cb = 0; cb < 16; ++cb) st.o[cb][0] = st.o[cb][1] = st.o[cb][2] = st.o[cb][3] = 0.f;
   st.mterm[0] = st.mterm[1] = 0.f;
   st.m_run = -INFINITY;
-  st.l_run = 0.f;
+  st.l_part = 0.f;
 
   const bool is_bf16 = split == p.n_split;
   if (is_bf16) bf16_split(p, sh, b, T, qa, qra, st, flags);
@@ -561,11 +597,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
     *reinterpret_cast<float2*>(o1 + 8 * cb + 2 * q) =
         make_float2(oscale * st.o[cb][2] + mt1, oscale * st.o[cb][3] + mt1);
   }
+  float l_run = st.l_part;
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, o);
   if ((lane & 7) == 0) {
     const int hh = h0 + 4 * warp + (lane >> 3);
     float* ml = p.ml_part + ((static_cast<size_t>(b) * p.H + hh) * NS + split) * 2;
     ml[0] = st.m_run;
-    ml[1] = st.l_run;
+    ml[1] = l_run;
   }
   flags = __reduce_or_sync(0xffffffffu, flags);
   if (lane == 0 && flags) atomicOr(p.err, flags);

@@ -98,8 +98,19 @@ __device__ __forceinline__ int find_seq(const int32_t* cu, int B, int r) {
 
 // ------------------------------------------------------------------ per-token work (one warp)
 __device__ void write_token(const WriteParams& p, int r, int lane) {
-  const int b = find_seq(p.cu_new, p.B, r);
-  const int r0 = __ldg(p.cu_new + b), r1 = __ldg(p.cu_new + b + 1);
+  // decode steps write one row per sequence (cu_new[b] = b): then row r belongs to sequence r,
+  // found with two independent loads instead of a dependent binary search
+  int b = -1, r0 = 0, r1 = 0;
+  if (r < p.B) {
+    r0 = __ldg(p.cu_new + r);
+    r1 = __ldg(p.cu_new + r + 1);
+    if (r0 == r && r1 == r + 1) b = r;
+  }
+  if (b < 0) {
+    b = find_seq(p.cu_new, p.B, r);
+    r0 = __ldg(p.cu_new + b);
+    r1 = __ldg(p.cu_new + b + 1);
+  }
   if (r < r0 || r >= r1) {  // inconsistent row offsets
     if (lane == 0) raise_err(p.err, kErrRows);
     return;
