@@ -26,6 +26,7 @@ namespace mlaq {
 namespace {
 
 constexpr int kThreads = 128;
+constexpr int kCtasPerSm = 3;  // resident CTAs per SM the register budget is sized for
 constexpr int kStages = 8;
 constexpr int kTile = 16;
 constexpr int kRowStride = 24;              // floats per head row in the score / P exchange
@@ -90,17 +91,16 @@ struct State {
   float l_part;    // this lane's share of the running sum (reduced over the 8 lanes at the end)
 };
 
-// Exchange the warps' partial scores, run the online softmax for 4 heads per warp, publish
-// P and (when some head's reference max moved) the rescale factors. Two CTA barriers; returns
-// true if any thread saw a timeout. sh.strict[buf] (a CTA-wide flag for this sub-tile) forces
-// an exact running max so that every weight stays <= 1.
+// First half of the exchange: publish this warp's partial scores (first CTA barrier). Returns
+// true if any thread saw a timeout. sh.strict[buf] (a CTA-wide flag for this sub-tile, read in
+// the second half) forces an exact running max so that every weight stays <= 1.
 //
 // Lazy rescaling: the reference max of a head moves only when a tile exceeds it by more than
 // kRescaleSlack (log2 units), so the weights stay <= 2^kRescaleSlack, the accumulators are
 // rescaled rarely and the common path needs no cross-lane reduction. The result does not
 // depend on the reference (it cancels in O / l and is accounted for in the LSE).
-__device__ __forceinline__ bool exchange_softmax(const Shared& sh, int buf, const float (&part)[2][4], int t0,
-                                                 int lo, int hi, float scale_log2, State& st, bool timed_out) {
+__device__ __forceinline__ bool exchange_partials(const Shared& sh, int buf, const float (&part)[2][4],
+                                                  bool timed_out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
   float* my = sh.sbuf + (buf * 4 + warp) * 16 * kRowStride;
 #pragma unroll
@@ -108,7 +108,14 @@ __device__ __forceinline__ bool exchange_softmax(const Shared& sh, int buf, cons
     *reinterpret_cast<float2*>(my + g * kRowStride + 8 * nb + 2 * q) = make_float2(part[nb][0], part[nb][1]);
     *reinterpret_cast<float2*>(my + (g + 8) * kRowStride + 8 * nb + 2 * q) = make_float2(part[nb][2], part[nb][3]);
   }
-  if (__syncthreads_or(timed_out)) return true;
+  return __syncthreads_or(timed_out) != 0;
+}
+
+// Second half: the online softmax of 4 heads per warp over the summed partials, P published
+// for all warps (second CTA barrier), accumulators rescaled if some reference max moved.
+__device__ __forceinline__ void softmax_publish(const Shared& sh, int buf, int t0, int lo, int hi, float scale_log2,
+                                                State& st) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2;
   const bool strict = sh.strict[buf] != 0;
 
   const int hh = 4 * warp + (lane >> 3), tt = 2 * (lane & 7);
@@ -161,7 +168,6 @@ __device__ __forceinline__ bool exchange_softmax(const Shared& sh, int buf, cons
     st.mterm[0] *= a0;
     st.mterm[1] *= a1;
   }
-  return false;
 }
 
 // P fragment (rows g, g+8; tokens 2q,2q+1 and 2q+8,2q+9) from the published P.
@@ -208,23 +214,33 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
   constexpr int kStageBytes = packed_stage_bytes(BITS);
   constexpr int kLatBytes = kTile * 64 * BITS;
   const uint8_t* pool = p.pool;
-  auto issue = [&](int i) {
+  // Stage i is filled by four bulk copies, one issued by lane 0 of each warp (the stage's
+  // mbarrier expects four arrivals), so no warp carries the whole producer load.
+  auto issue_part = [&](int i, int part) {
     const int k = sub_begin + i;
     const int pg = k * kTile / p.P, tp0 = (k * kTile) % p.P;
     const int32_t pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
     const uint8_t* base = pool + static_cast<size_t>(pid) * static_cast<size_t>(p.page_bytes);
     uint8_t* dst = sh.stages + (i % kStages) * kStageBytes;
     uint64_t* bar = sh.bars + (i % kStages);
-    mbar_arrive_expect_tx(bar, kStageBytes);
-    bulk_g2s(dst, base + (tp0 / 8) * 4 * (128 * BITS), kLatBytes, bar);
-    bulk_g2s(dst + kLatBytes, base + static_cast<size_t>(p.P) * 64 * BITS + (tp0 / 16) * 512, 512, bar);
-    bulk_g2s(dst + kLatBytes + 512, base + static_cast<size_t>(p.P) * (64 * BITS + 32) + tp0 * 16, 256, bar);
-    bulk_g2s(dst + kLatBytes + 768, base + static_cast<size_t>(p.P) * (64 * BITS + 48), 256, bar);
+    if (part == 0) {
+      mbar_arrive_expect_tx(bar, kLatBytes);
+      bulk_g2s(dst, base + (tp0 / 8) * 4 * (128 * BITS), kLatBytes, bar);
+    } else if (part == 1) {
+      mbar_arrive_expect_tx(bar, 512);
+      bulk_g2s(dst + kLatBytes, base + static_cast<size_t>(p.P) * 64 * BITS + (tp0 / 16) * 512, 512, bar);
+    } else if (part == 2) {
+      mbar_arrive_expect_tx(bar, 256);
+      bulk_g2s(dst + kLatBytes + 512, base + static_cast<size_t>(p.P) * (64 * BITS + 32) + tp0 * 16, 256, bar);
+    } else {
+      mbar_arrive_expect_tx(bar, 256);
+      bulk_g2s(dst + kLatBytes + 768, base + static_cast<size_t>(p.P) * (64 * BITS + 48), 256, bar);
+    }
   };
-  int issued = 0;  // meaningful in thread 0 only
-  if (threadIdx.x == 0) {
-    for (; issued < kStages && issued < n_my; ++issued) issue(issued);
-  }
+  int issued = 0;  // identical in every thread
+  if (lane == 0)
+    for (int i = 0; i < kStages && i < n_my; ++i) issue_part(i, warp);
+  issued = n_my < kStages ? n_my : kStages;
 
   // per-page rope factors: query times channel scale split into two BF16 terms
   uint32_t qr_hi[4], qr_lo[4];
@@ -315,11 +331,12 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
     // four independent accumulation chains per n-block pair keep the tensor pipe busy
     float acc[2][4], acc1[2][4], racc[2][4];
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb)
+    for (int nb = 0; nb < 2; ++nb) {
+      mma_bf16_16816_z(acc[nb], qa[0], bq[nb][0][0], bq[nb][0][1]);
+      mma_bf16_16816_z(acc1[nb], qa[1], bq[nb][1][0], bq[nb][1][1]);
+    }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[nb][e] = acc1[nb][e] = racc[nb][e] = 0.f;
-#pragma unroll
-    for (int kc = 0; kc < 8; kc += 2)
+    for (int kc = 2; kc < 8; kc += 2)
 #pragma unroll
       for (int nb = 0; nb < 2; ++nb) {
         mma_bf16_16816(acc[nb], qa[kc], bq[nb][kc][0], bq[nb][kc][1]);
@@ -327,7 +344,7 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
       }
 #pragma unroll
     for (int nb = 0; nb < 2; ++nb) {
-      mma_bf16_16816(racc[nb], qr_hi, rb[nb][0], rb[nb][1]);
+      mma_bf16_16816_z(racc[nb], qr_hi, rb[nb][0], rb[nb][1]);
       mma_bf16_16816(racc[nb], qr_lo, rb[nb][0], rb[nb][1]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[nb][e] += acc1[nb][e];
@@ -365,7 +382,7 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
 #pragma unroll
         for (int nb = 0; nb < 2; ++nb) bq[nb][kc][r] = hsub2_u32(movmatrix_t(bq[nb][kc][r]), 0x43004300u);
 
-    if (exchange_softmax(sh, buf, part, t0, lo, hi, p.scale_log2, st, !ok)) {
+    if (exchange_partials(sh, buf, part, !ok)) {
       flags |= kErrTimeout;
       // orderly exit: bounded waits for the copies still in flight into this CTA
       if (threadIdx.x == 0)
@@ -374,11 +391,14 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
       break;
     }
     // the previous stage is free once every warp passed the first exchange barrier
-    if (threadIdx.x == 0 && i >= 1 && issued < n_my) {
-      fence_proxy_async_smem();
-      issue(issued);
+    if (i >= 1 && issued < n_my) {
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        issue_part(issued, warp);
+      }
       ++issued;
     }
+    softmax_publish(sh, buf, t0, lo, hi, p.scale_log2, st);
 
     // ---- readout: A = P * token scale (FP16), B = codes / 512 (FP16, exact)
     float2 pf[4];
@@ -469,13 +489,14 @@ __device__ void bf16_split(const DecodeParams& p, const Shared& sh, int b, int T
 
     const int buf = i & 1;
     // positions are relative to the tile start: valid rows are [0, count)
-    if (exchange_softmax(sh, buf, part, 0, 0, count, p.scale_log2, st, !ok)) {
+    if (exchange_partials(sh, buf, part, !ok)) {
       flags |= kErrTimeout;
       if (threadIdx.x == 0)
         for (int j = i; j < min(i + 2, n_tiles); ++j)
           (void)mbar_wait_bounded(sh.bars + (j & 1), (j >> 1) & 1, kWaitBudget >> 4);
       break;
     }
+    softmax_publish(sh, buf, 0, 0, count, p.scale_log2, st);
     float2 pf[4];
     load_p(sh, buf, pf);
     uint32_t ah[4], al[4];
@@ -507,7 +528,7 @@ __device__ void bf16_split(const DecodeParams& p, const Shared& sh, int b, int T
 }
 
 template <int BITS>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const Shared sh = carve<BITS>(smem);
   const int split = blockIdx.x, hb = blockIdx.y, b = blockIdx.z;
@@ -521,7 +542,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
     T = 0;
   }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) mbar_init(sh.bars + i, 1);
+    // packed stages: four arrivals (one copy per warp); protected-token stages: one arrival
+    for (int i = 0; i < kStages; ++i) mbar_init(sh.bars + i, split == p.n_split ? 1 : 4);
     fence_mbar_init();
     sh.strict[0] = sh.strict[1] = 0;
   }
@@ -654,7 +676,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p) {
 
 int decode_num_splits(int B, int H, int max_pages, int P, int num_sms) {
   const int groups = B * (H / 16);
-  const int target = 2 * num_sms;
+  const int target = kCtasPerSm * num_sms;  // one full wave of resident CTAs
   int ns = target / (groups > 0 ? groups : 1) - 1;
   const long long max_sub = (static_cast<long long>(max_pages) * P) / kTile;
   int cap = static_cast<int>(max_sub / 4);
