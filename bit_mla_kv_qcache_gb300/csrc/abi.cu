@@ -163,6 +163,8 @@ int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H, c
   p.H = H;
   p.max_pages = max_pages;
   p.P = cfg->page_size;
+  p.p_shift = 0;
+  while ((1 << p.p_shift) < p.P) ++p.p_shift;
   p.S = cfg->n_sink;
   p.W = cfg->n_recent;
   p.bits_c = cfg->bits_c;

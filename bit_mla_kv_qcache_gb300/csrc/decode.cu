@@ -198,8 +198,8 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
   // validate the page ids this split reads; a bad id drops the split's work
   {
     bool bad = false;
-    const int pg0 = sub_begin * kTile / p.P;
-    const int pg1 = n_my > 0 ? ((sub_begin + n_my) * kTile - 1) / p.P : pg0 - 1;
+    const int pg0 = (sub_begin * kTile) >> p.p_shift;
+    const int pg1 = n_my > 0 ? (((sub_begin + n_my) * kTile - 1) >> p.p_shift) : pg0 - 1;
     for (int pg = pg0 + static_cast<int>(threadIdx.x); pg <= pg1; pg += kThreads) {
       const int32_t pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
       bad |= pid < 0 || pid >= p.n_pages;
@@ -218,7 +218,7 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
   // mbarrier expects four arrivals), so no warp carries the whole producer load.
   auto issue_part = [&](int i, int part) {
     const int k = sub_begin + i;
-    const int pg = k * kTile / p.P, tp0 = (k * kTile) % p.P;
+    const int pg = (k * kTile) >> p.p_shift, tp0 = (k * kTile) & (p.P - 1);
     const int32_t pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
     const uint8_t* base = pool + static_cast<size_t>(pid) * static_cast<size_t>(p.page_bytes);
     uint8_t* dst = sh.stages + (i % kStages) * kStageBytes;
@@ -252,7 +252,7 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
     const bool ok = mbar_wait_bounded(sh.bars + stg, (i / kStages) & 1, kWaitBudget);
     const uint8_t* sp = sh.stages + stg * kStageBytes;
     const int k = sub_begin + i, t0 = k * kTile;
-    const int pg = t0 / p.P;
+    const int pg = t0 >> p.p_shift;
     if (pg != cur_pg) {
       cur_pg = pg;
       const uint32_t* rm = reinterpret_cast<const uint32_t*>(sp + kLatBytes + 768) + 16 * warp;

@@ -58,6 +58,7 @@ struct DecodeParams {
   int64_t page_bytes;
   float scale_log2;  // softmax_scale * log2(e)
   int B, H, max_pages, P, S, W, bits_c;
+  int p_shift;  // log2(P): page sizes are powers of two
   int n_split;  // splits of the packed tokens; split index n_split is the BF16 (protected) split
 };
 
