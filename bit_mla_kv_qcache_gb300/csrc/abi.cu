@@ -96,7 +96,7 @@ int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, co
   p.sink = sink_buf;
   p.ring = recent_buf;
   p.err = err_word;
-  const int token_blocks = (n_rows + 3) / 4;
+  const int token_blocks = n_rows;  // one CTA per new token
   const int fill_per_seq = max_new / p.P + 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;

@@ -34,7 +34,7 @@ struct WriteParams {
   uint16_t* sink;
   uint16_t* ring;
   int32_t* err;
-  int token_blocks;  // blocks [0, token_blocks) do per-token work (4 tokens per block)
+  int token_blocks;  // blocks [0, token_blocks) do per-token work (one token per block)
   int fill_per_seq;  // page-fill blocks per sequence after the token blocks
 };
 

@@ -1,6 +1,6 @@
 // Fused cache writer (QuantMLA page, appendix Figure 8; RAQ-MLA page, appendix Table 5).
 //
-// Per new token (one warp each): BF16 retention in the sink buffer / recent ring, per-token
+// Per new token (one CTA each): BF16 retention in the sink buffer / recent ring, per-token
 // clip of the latent at a nearest-rank quantile of |c|, per-128-channel-group quantization
 // with an FP16 minimum (rounded down) and FP16 scale (rounded up), and the bit-packed store
 // into the token's page slot. Per page that fills during the call (one CTA each): per-channel
@@ -96,8 +96,11 @@ __device__ __forceinline__ int find_seq(const int32_t* cu, int B, int r) {
   return lo;
 }
 
-// ------------------------------------------------------------------ per-token work (one warp)
-__device__ void write_token(const WriteParams& p, int r, int lane) {
+// ------------------------------------------------------------------ per-token work (one CTA)
+// 128 threads per new token: warp w owns latent group w (channels 128w..128w+127, four per
+// lane); lanes of warp 0 also carry the token's k_R (two channels each) for the retention copy.
+__device__ void write_token(const WriteParams& p, int r, int (&s_cnt)[2][4]) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // decode steps write one row per sequence (cu_new[b] = b): then row r belongs to sequence r,
   // found with two independent loads instead of a dependent binary search
   int b = -1, r0 = 0, r1 = 0;
@@ -111,152 +114,137 @@ __device__ void write_token(const WriteParams& p, int r, int lane) {
     r0 = __ldg(p.cu_new + b);
     r1 = __ldg(p.cu_new + b + 1);
   }
-  if (r < r0 || r >= r1) {  // inconsistent row offsets
-    if (lane == 0) raise_err(p.err, kErrRows);
+  if (r < r0 || r >= r1 || r1 - r0 > p.max_new) {  // inconsistent row offsets
+    if (tid == 0) raise_err(p.err, kErrRows);
     return;
   }
   const int n_b = r1 - r0;
-  if (n_b > p.max_new) {
-    if (lane == 0) raise_err(p.err, kErrRows);
-    return;
-  }
   const int s0 = __ldg(p.seq_lens + b);
   if (s0 < 0) {
-    if (lane == 0) raise_err(p.err, kErrSeqOverflow);
+    if (tid == 0) raise_err(p.err, kErrSeqOverflow);
     return;
   }
   const int64_t t = static_cast<int64_t>(s0) + (r - r0);
   const int64_t t_final = static_cast<int64_t>(s0) + n_b;
 
-  // ---- load: lane holds latent channels [16*lane, 16*lane+16) and k_R channels [2*lane, 2*lane+2)
-  const uint4* crow = reinterpret_cast<const uint4*>(p.c_new + static_cast<size_t>(r) * kLatent) + 2 * lane;
-  const uint4 c0 = __ldg(crow), c1 = __ldg(crow + 1);
-  const uint32_t kr2 = __ldg(reinterpret_cast<const uint32_t*>(p.kr_new + static_cast<size_t>(r) * kRope) + lane);
+  // ---- load: thread holds latent channels [4*tid, 4*tid+4); warp 0 lanes k_R [2*lane, 2*lane+2)
+  const uint2 cv = __ldg(reinterpret_cast<const uint2*>(p.c_new + static_cast<size_t>(r) * kLatent) + tid);
+  uint32_t kr2 = 0;
+  if (warp == 0) kr2 = __ldg(reinterpret_cast<const uint32_t*>(p.kr_new + static_cast<size_t>(r) * kRope) + lane);
 
   // ---- BF16 retention (pre-quantization values)
   if (t < p.S) {
     uint16_t* row = p.sink + (static_cast<size_t>(b) * p.S + t) * kRow;
-    reinterpret_cast<uint4*>(row)[2 * lane] = c0;
-    reinterpret_cast<uint4*>(row)[2 * lane + 1] = c1;
-    reinterpret_cast<uint32_t*>(row + kLatent)[lane] = kr2;
+    reinterpret_cast<uint2*>(row)[tid] = cv;
+    if (warp == 0) reinterpret_cast<uint32_t*>(row + kLatent)[lane] = kr2;
   }
   if (t >= t_final - p.W) {
     uint16_t* row = p.ring + (static_cast<size_t>(b) * p.W + (t % p.W)) * kRow;
-    reinterpret_cast<uint4*>(row)[2 * lane] = c0;
-    reinterpret_cast<uint4*>(row)[2 * lane + 1] = c1;
-    reinterpret_cast<uint32_t*>(row + kLatent)[lane] = kr2;
+    reinterpret_cast<uint2*>(row)[tid] = cv;
+    if (warp == 0) reinterpret_cast<uint32_t*>(row + kLatent)[lane] = kr2;
   }
 
   // ---- page slot
   const int64_t pg = t / p.P;
   if (pg >= p.max_pages) {
-    if (lane == 0) raise_err(p.err, kErrSeqOverflow);
+    if (tid == 0) raise_err(p.err, kErrSeqOverflow);
     return;
   }
   const int32_t pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
   if (pid < 0 || pid >= p.n_pages) {
-    if (lane == 0) raise_err(p.err, kErrBadPage);
+    if (tid == 0) raise_err(p.err, kErrBadPage);
     return;
   }
   const int tp = static_cast<int>(t % p.P);
   uint8_t* page = p.pool + static_cast<size_t>(pid) * static_cast<size_t>(p.page_bytes);
 
-  float x[16];
-  const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    x[2 * i] = bf16_lo(cw[i]);
-    x[2 * i + 1] = bf16_hi(cw[i]);
-  }
-  int flags = 0;
+  float x[4] = {bf16_lo(cv.x), bf16_hi(cv.x), bf16_lo(cv.y), bf16_hi(cv.y)};
   bool bad = false;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) bad |= !isfinite(x[i]);
-  if (__any_sync(0xffffffffu, bad)) flags |= kErrNonFinite;
+  for (int i = 0; i < 4; ++i) bad |= !isfinite(x[i]);
+  int flags = __syncthreads_or(bad) ? kErrNonFinite : 0;
 
-  // ---- per-token clip: tau = clip_k-th smallest |x| (nearest-rank order statistic)
+  // ---- per-token clip: tau = clip_k-th smallest |x| over the 512 channels (nearest rank),
+  // found by bisection on the BF16 magnitude bit patterns, counts reduced across the CTA
   if (p.clip_k > 0) {
-    uint32_t key[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      key[2 * i] = cw[i] & 0x7fffu;
-      key[2 * i + 1] = (cw[i] >> 16) & 0x7fffu;
-    }
+    const uint32_t key[4] = {cv.x & 0x7fffu, (cv.x >> 16) & 0x7fffu, cv.y & 0x7fffu, (cv.y >> 16) & 0x7fffu};
     uint32_t lo = 0, hi = 0x7fffu;
+    int it = 0;
     while (lo < hi) {
       const uint32_t mid = (lo + hi) >> 1;
-      int cnt = 0;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) cnt += key[i] <= mid;
+      int cnt = (key[0] <= mid) + (key[1] <= mid) + (key[2] <= mid) + (key[3] <= mid);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-      if (cnt >= p.clip_k) hi = mid;
+      if (lane == 0) s_cnt[it & 1][warp] = cnt;
+      __syncthreads();
+      const int total = s_cnt[it & 1][0] + s_cnt[it & 1][1] + s_cnt[it & 1][2] + s_cnt[it & 1][3];
+      if (total >= p.clip_k) hi = mid;
       else lo = mid + 1;
+      ++it;
     }
     const float tau = __uint_as_float(lo << 16);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = fminf(fmaxf(x[i], -tau), tau);
+    for (int i = 0; i < 4; ++i) x[i] = fminf(fmaxf(x[i], -tau), tau);
   }
 
-  // ---- group statistics over lanes [8g, 8g+8)
-  float lo = x[0], hi = x[0];
+  // ---- group statistics over the warp
+  float lo = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+  float hi = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
 #pragma unroll
-  for (int i = 1; i < 16; ++i) {
-    lo = fminf(lo, x[i]);
-    hi = fmaxf(hi, x[i]);
-  }
-#pragma unroll
-  for (int o = 1; o < 8; o <<= 1) {
+  for (int o = 1; o < 32; o <<= 1) {
     lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
     hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
   }
   const int L = (1 << p.bits_c) - 1;
   const QParams qp = make_qparams(lo, hi, L);
   flags |= qp.flags;
-
-  int code[16];
+  int code[4];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) code[i] = quant_code(x[i], qp.m, qp.s, qp.inv_s, L);
+  for (int i = 0; i < 4; ++i) code[i] = quant_code(x[i], qp.m, qp.s, qp.inv_s, L);
 
-  // ---- pack into the documented fragment layout (region A)
-  const int g = lane >> 3, k = lane & 7;
-  uint8_t* blk = page + static_cast<size_t>(((tp >> 3) * 4 + g) * (128 * p.bits_c));
+  // ---- pack into the documented fragment layout (region A). This lane holds chunk k = lane/4
+  // (16 channels), positions e = 4m + i of it (m = lane%4): it feeds the words of lanes
+  // q = 2(m%2) + d (d = 0: e = 4m, 4m+1; d = 1: e = 4m+2, 4m+3), h = m/2.
+  const int k = lane >> 2, m = lane & 3, h = m >> 1;
+  uint8_t* blk = page + static_cast<size_t>(((tp >> 3) * 4 + warp) * (128 * p.bits_c));
   const int lane_base = 4 * (tp & 7);
   if (p.bits_c == 4) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t w = 0;
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int o = 0; o < 2; ++o)
-          w |= static_cast<uint32_t>(code[8 * h + 2 * q + o]) << (4 * (2 * (k & 1) + h + 4 * o));
-      w |= __shfl_xor_sync(0xffffffffu, w, 1);
-      if ((k & 1) == 0)
-        *reinterpret_cast<uint32_t*>(blk + (lane_base + q) * 16 + (k >> 1) * 4) = w;
+    const int sft = 2 * (k & 1) + h;
+    uint32_t w0 = (static_cast<uint32_t>(code[0]) << (4 * sft)) | (static_cast<uint32_t>(code[1]) << (4 * (sft + 4)));
+    uint32_t w1 = (static_cast<uint32_t>(code[2]) << (4 * sft)) | (static_cast<uint32_t>(code[3]) << (4 * (sft + 4)));
+    // a word gathers chunks 2j, 2j+1 and h = 0, 1: lanes differing in bits 1 and 2
+    w0 |= __shfl_xor_sync(0xffffffffu, w0, 2);
+    w1 |= __shfl_xor_sync(0xffffffffu, w1, 2);
+    w0 |= __shfl_xor_sync(0xffffffffu, w0, 4);
+    w1 |= __shfl_xor_sync(0xffffffffu, w1, 4);
+    if ((lane & 6) == 0) {
+      const int q0 = 2 * (m & 1), j = k >> 1;
+      *reinterpret_cast<uint32_t*>(blk + (lane_base + q0) * 16 + j * 4) = w0;
+      *reinterpret_cast<uint32_t*>(blk + (lane_base + q0 + 1) * 16 + j * 4) = w1;
     }
   } else {
+    const int sft = 2 * (k & 3) + h;
+    uint32_t w0 = (static_cast<uint32_t>(code[0]) << (2 * sft)) | (static_cast<uint32_t>(code[1]) << (2 * (sft + 8)));
+    uint32_t w1 = (static_cast<uint32_t>(code[2]) << (2 * sft)) | (static_cast<uint32_t>(code[3]) << (2 * (sft + 8)));
+    // a word gathers chunks 4j..4j+3 and h = 0, 1: lanes differing in bits 1, 2 and 3
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t w = 0;
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int o = 0; o < 2; ++o)
-          w |= static_cast<uint32_t>(code[8 * h + 2 * q + o]) << (2 * (2 * (k & 3) + h + 8 * o));
-      w |= __shfl_xor_sync(0xffffffffu, w, 1);
-      w |= __shfl_xor_sync(0xffffffffu, w, 2);
-      if ((k & 3) == 0)
-        *reinterpret_cast<uint32_t*>(blk + (lane_base + q) * 8 + (k >> 2) * 4) = w;
+    for (int o = 2; o <= 8; o <<= 1) {
+      w0 |= __shfl_xor_sync(0xffffffffu, w0, o);
+      w1 |= __shfl_xor_sync(0xffffffffu, w1, o);
+    }
+    if ((lane & 14) == 0) {
+      const int q0 = 2 * (m & 1), j = k >> 2;
+      *reinterpret_cast<uint32_t*>(blk + (lane_base + q0) * 8 + j * 4) = w0;
+      *reinterpret_cast<uint32_t*>(blk + (lane_base + q0 + 1) * 8 + j * 4) = w1;
     }
   }
   // ---- latent metadata (region C)
-  if (k == 0) {
-    uint8_t* meta = page + static_cast<size_t>(p.P) * (64 * p.bits_c + 32) + (tp * 4 + g) * 4;
+  if (lane == 0) {
+    uint8_t* meta = page + static_cast<size_t>(p.P) * (64 * p.bits_c + 32) + (tp * 4 + warp) * 4;
     *reinterpret_cast<uint32_t*>(meta) = qp.meta;
   }
   flags = __reduce_or_sync(0xffffffffu, flags);
-  if (lane == 0) raise_err(p.err, flags);
+  if (lane == 0 && flags) raise_err(p.err, flags);
 }
 
 // ------------------------------------------------------------------ page fill (one CTA)
@@ -334,8 +322,8 @@ __global__ void __launch_bounds__(128) write_kernel(const WriteParams p) {
     if (__ldg(p.cu_new) != 0 || __ldg(p.cu_new + p.B) != p.n_rows) raise_err(p.err, kErrRows);
   }
   if (static_cast<int>(blockIdx.x) < p.token_blocks) {
-    const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
-    if (r < p.n_rows) write_token(p, r, threadIdx.x & 31);
+    __shared__ int s_cnt[2][4];
+    write_token(p, blockIdx.x, s_cnt);
     return;
   }
   const int idx = blockIdx.x - p.token_blocks;
