@@ -32,6 +32,7 @@ constexpr int kTile = 16;
 constexpr int kRowStride = 24;              // floats per head row in the score / P exchange
 constexpr int kBf16RowBytes = kRow * 2 + 16;  // padded BF16 row in shared memory (1168 B)
 constexpr long long kWaitBudget = 4ll << 30;  // ~2 s at 2 GHz before a wait gives up
+constexpr int kMaxSplitPages = 512;          // page ids of a split cached in shared memory
 constexpr float kRescaleSlack = 8.f;          // softmax weights stay <= 2^8 between rescales
 constexpr float kStrictScale = 255.f;         // a token scale >= this forces weights <= 1 (FP16 safety)
 
@@ -43,7 +44,8 @@ __host__ __device__ constexpr int stage_region_bytes(int bits) {
 constexpr int kSbufFloats = 2 * 4 * 16 * kRowStride;
 constexpr int kPbufFloats = 2 * 16 * kRowStride;
 __host__ __device__ constexpr int smem_bytes(int bits) {
-  return stage_region_bytes(bits) + (kSbufFloats + kPbufFloats + 2 * 16) * 4 + kStages * 8 + 2 * 4;
+  return stage_region_bytes(bits) + (kSbufFloats + kPbufFloats + 2 * 16) * 4 + kStages * 8 + 2 * 4 +
+         kMaxSplitPages * 4;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -69,6 +71,7 @@ struct Shared {
   float* alpha;  // [2][16]
   uint64_t* bars;
   int* strict;   // [2] per exchange buffer: a sub-tile needs an exact running max
+  int* pids;     // [kMaxSplitPages] physical page ids of the split's pages (packed path)
 };
 
 template <int BITS>
@@ -80,6 +83,7 @@ __device__ __forceinline__ Shared carve(uint8_t* smem) {
   s.alpha = s.pbuf + kPbufFloats;
   s.bars = reinterpret_cast<uint64_t*>(s.alpha + 2 * 16);
   s.strict = reinterpret_cast<int*>(s.bars + kStages);
+  s.pids = s.strict + 2;
   return s;
 }
 
@@ -203,6 +207,7 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
     for (int pg = pg0 + static_cast<int>(threadIdx.x); pg <= pg1; pg += kThreads) {
       const int32_t pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
       bad |= pid < 0 || pid >= p.n_pages;
+      if (pg - pg0 < kMaxSplitPages) sh.pids[pg - pg0] = pid;  // refills read ids from here
     }
     if (__syncthreads_or(bad)) {
       flags |= kErrBadPage;
@@ -219,7 +224,9 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
   auto issue_part = [&](int i, int part) {
     const int k = sub_begin + i;
     const int pg = (k * kTile) >> p.p_shift, tp0 = (k * kTile) & (p.P - 1);
-    const int32_t pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
+    const int pg0 = (sub_begin * kTile) >> p.p_shift;
+    const int32_t pid = pg - pg0 < kMaxSplitPages ? sh.pids[pg - pg0]
+                                                 : __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
     const uint8_t* base = pool + static_cast<size_t>(pid) * static_cast<size_t>(p.page_bytes);
     uint8_t* dst = sh.stages + (i % kStages) * kStageBytes;
     uint64_t* bar = sh.bars + (i % kStages);
