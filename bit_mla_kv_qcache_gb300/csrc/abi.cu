@@ -17,7 +17,7 @@ int check_config(const mla_qcache_config* c) {
   if (c->bits_c != 2 && c->bits_c != 4) return MLA_QCACHE_ERR_CONFIG;
   if (c->bits_r != 4) return MLA_QCACHE_ERR_CONFIG;
   const int P = c->page_size;
-  if (P != 16 && P != 32 && P != 64 && P != 128) return MLA_QCACHE_ERR_CONFIG;
+  if (P != 32 && P != 64 && P != 128) return MLA_QCACHE_ERR_CONFIG;  // a 32-token decode tile never straddles pages
   if (c->n_sink < 0 || c->n_sink > 16) return MLA_QCACHE_ERR_CONFIG;
   if (c->n_recent < P || c->n_recent > 1024) return MLA_QCACHE_ERR_CONFIG;
   if (!(c->clip_q >= 0.0f && c->clip_q <= 1.0f)) return MLA_QCACHE_ERR_CONFIG;

@@ -2,20 +2,28 @@
 // Figure 8; RAQ-MLA page, Figures 3-4 and appendix Table 5).
 //
 // Grid (n_split + 1, H/16, B). CTA (s, hb, b) handles 16 heads of sequence b:
-//   s <  n_split : an even share of the packed tokens [S, T-W), streamed 16 tokens at a time
+//   s <  n_split : an even share of the packed tokens [S, T-W), in tiles of 32 tokens streamed
 //                  from the page pool into a ring of shared-memory stages by bulk copies;
 //   s == n_split : the protected tokens (t < S or t >= T-W) from the BF16 sink/recent buffers.
 // Each CTA writes an unnormalized partial (O, max, sum); a second kernel merges the partials
 // with a log-sum-exp reduction (one global softmax over all tokens).
 //
-// Inside a CTA, warp w owns latent group w (channels 128w..128w+127) and k_R chunk w
-// (channels 16w..16w+15). Packed codes are never dequantized into a tile:
+// Packed tiles. Warp w owns latent group w (channels 128w..128w+127) and k_R chunk w
+// (channels 16w..16w+15). Codes are never dequantized into a tile:
 //   scores:  q . c_hat = scale_t * sum_i q_i code_ti + min_t * sum_i q_i  (per token group),
-//            computed on tensor cores with the codes as exact small integers;
 //   readout: sum_t p_t c_hat_t = sum_t (p_t scale_t) code_t + sum_t p_t min_t,
-//            the same codes transposed in registers (movmatrix) as the B operand.
-// k_R uses its per-page channel scale folded into the query (split into two BF16 terms so the
-// product stays accurate to ~2^-16).
+// both on tensor cores. The codes reach the products as FP16 subnormals: the bit pattern n
+// (or 16n, 4^i n) of a 16-bit half is the exact value n * 2^-24 (times that power of two), so
+// a single AND of a code word yields a ready operand. Matrix loads (ldmatrix) read 8x8 blocks
+// of 16-bit elements straight from the staged token-major rows: plain for the score operand
+// (token columns), transposed for the readout operand (token rows). The query is converted to
+// FP16 with a per-head power-of-two prescale (exact for BF16 inputs) and permuted to match the
+// channel order the masks produce. k_R uses its per-page channel scale folded into the query
+// (split into two BF16 terms so the product stays accurate to ~2^-16).
+//
+// Within a CTA the four warps exchange partial scores through shared memory; the exchanges
+// are skewed over mbarriers so that the scores of tile i+1 are computed while the softmax of
+// tile i is still being published.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -26,27 +34,49 @@ namespace mlaq {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kCtasPerSm = 3;  // resident CTAs per SM the register budget is sized for
-constexpr int kStages = 8;
-constexpr int kTile = 16;
-constexpr int kRowStride = 24;              // floats per head row in the score / P exchange
+constexpr int kCtasPerSm = 3;  // resident CTAs per SM the register and shared budgets are sized for
+constexpr int kPT = 32;        // tokens per packed tile
+constexpr int kTile = 16;      // tokens per protected (BF16) tile
+constexpr int kRowStride = 24;              // floats per head row in the BF16-path exchange
+constexpr int kXStride = 40;                // floats per head row in the packed-path exchange
+constexpr int kOutStride = 516;             // floats per head row when staging the partial output
 constexpr int kBf16RowBytes = kRow * 2 + 16;  // padded BF16 row in shared memory (1168 B)
 constexpr long long kWaitBudget = 4ll << 30;  // ~2 s at 2 GHz before a wait gives up
 constexpr int kMaxSplitPages = 512;          // page ids of a split cached in shared memory
 constexpr float kRescaleSlack = 8.f;          // softmax weights stay <= 2^8 between rescales
 constexpr float kStrictScale = 255.f;         // a token scale >= this forces weights <= 1 (FP16 safety)
 
-__host__ __device__ constexpr int packed_stage_bytes(int bits) { return kTile * 64 * bits + 512 + 256 + 256; }
-__host__ __device__ constexpr int stage_region_bytes(int bits) {
-  return (kStages * packed_stage_bytes(bits) > 2 * kTile * kBf16RowBytes) ? kStages * packed_stage_bytes(bits)
-                                                                          : 2 * kTile * kBf16RowBytes;
+__host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
+
+// Shared-memory stage of one packed tile: latent rows, k_R code blocks, latent metadata, k_R
+// metadata (the page layout's regions A-D restricted to the tile's 32 tokens).
+template <int BITS>
+struct Geom {
+  static constexpr int kRowBytes = 64 * BITS;
+  static constexpr int kLat = kPT * kRowBytes;
+  static constexpr int kRopeOff = kLat;             // 2 blocks of 16 tokens x 4 chunks x 128 B
+  static constexpr int kMetaOff = kLat + 1024;      // 32 tokens x 4 groups x (scale, min)
+  static constexpr int kRMetaOff = kMetaOff + 512;  // 64 channels x (scale, min)
+  static constexpr int kStage = kRMetaOff + 256;
+  static constexpr int kStages = BITS == 4 ? 4 : 7;
+  static constexpr int kRegion =
+      cmax(cmax(kStages * kStage, 2 * kTile * kBf16RowBytes), 16 * kOutStride * 4);
+};
+
+constexpr int kXsFloats = 2 * 4 * 16 * kXStride;  // partial scores [2 buf][4 warps][16 heads][32 tok]
+constexpr int kXpFloats = 2 * 16 * kXStride;      // weights [2 buf][16 heads][32 tok]
+constexpr int kNumBars = 12;                       // >= stages + 4 exchange barriers
+
+template <int BITS>
+__host__ __device__ constexpr int smem_bytes() {
+  return Geom<BITS>::kRegion + (kXsFloats + kXpFloats + 2 * 16 + 4 * 16) * 4 + kNumBars * 8 +
+         (2 * 4 + 2 * 4 + 2) * 4 + kMaxSplitPages * 4;
 }
-constexpr int kSbufFloats = 2 * 4 * 16 * kRowStride;
-constexpr int kPbufFloats = 2 * 16 * kRowStride;
-__host__ __device__ constexpr int smem_bytes(int bits) {
-  return stage_region_bytes(bits) + (kSbufFloats + kPbufFloats + 2 * 16) * 4 + kStages * 8 + 2 * 4 +
-         kMaxSplitPages * 4;
-}
+// kCtasPerSm CTAs (each with 1 KB reserved by the hardware) fit in an SM's 228 KB
+static_assert(kCtasPerSm * (smem_bytes<4>() + 1024) <= 228 * 1024 &&
+                  kCtasPerSm * (smem_bytes<2>() + 1024) <= 228 * 1024, "shared memory per SM");
+static_assert(Geom<4>::kStages + 4 <= kNumBars && Geom<2>::kStages + 4 <= kNumBars, "barriers");
+static_assert(2 * 4 * 16 * kRowStride <= kXsFloats && 2 * 16 * kRowStride <= kXpFloats, "BF16 exchange");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -56,40 +86,43 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   const __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
-__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
 __device__ __forceinline__ float half_lo(uint32_t w) { return __half2float(__ushort_as_half(static_cast<uint16_t>(w & 0xffffu))); }
 __device__ __forceinline__ float half_hi(uint32_t w) { return __half2float(__ushort_as_half(static_cast<uint16_t>(w >> 16))); }
+// 2^k as a float, k in [-126, 127]
+__device__ __forceinline__ float pow2i(int k) { return __uint_as_float(static_cast<uint32_t>(k + 127) << 23); }
 
 struct Shared {
-  uint8_t* stages;
-  float* sbuf;   // [2][4 warps][16 heads][kRowStride]
-  float* pbuf;   // [2][16 heads][kRowStride]
-  float* alpha;  // [2][16]
-  uint64_t* bars;
-  int* strict;   // [2] per exchange buffer: a sub-tile needs an exact running max
-  int* pids;     // [kMaxSplitPages] physical page ids of the split's pages (packed path)
+  uint8_t* stages;  // packed stages, or BF16 row stages, or the output staging tile
+  float* sbuf;      // packed: [2][4 warps][16 heads][kXStride]; BF16 path: [2][4][16][kRowStride]
+  float* pbuf;      // packed: [2][16 heads][kXStride]; BF16 path: [2][16][kRowStride]
+  float* alpha;     // [2][16]
+  float* qmax;      // [4 warps][16 heads]: per-warp query maxima (prologue)
+  uint64_t* bars;   // packed: stages full [kStages], scores ready [2], weights ready [2]
+  int* xflags;      // [2][4] per warp and tile: bit 0 strict (a token scale >= kStrictScale), bit 1 timeout
+  int* moved;       // [2][4] per warp and tile: a reference max moved (rescale the outputs)
+  int* strict;      // [2] BF16 path: per exchange buffer
+  int* pids;        // [kMaxSplitPages] physical page ids of the split's pages (packed path)
 };
 
 template <int BITS>
 __device__ __forceinline__ Shared carve(uint8_t* smem) {
   Shared s;
   s.stages = smem;
-  s.sbuf = reinterpret_cast<float*>(smem + stage_region_bytes(BITS));
-  s.pbuf = s.sbuf + kSbufFloats;
-  s.alpha = s.pbuf + kPbufFloats;
-  s.bars = reinterpret_cast<uint64_t*>(s.alpha + 2 * 16);
-  s.strict = reinterpret_cast<int*>(s.bars + kStages);
+  s.sbuf = reinterpret_cast<float*>(smem + Geom<BITS>::kRegion);
+  s.pbuf = s.sbuf + kXsFloats;
+  s.alpha = s.pbuf + kXpFloats;
+  s.qmax = s.alpha + 2 * 16;
+  s.bars = reinterpret_cast<uint64_t*>(s.qmax + 4 * 16);
+  s.xflags = reinterpret_cast<int*>(s.bars + kNumBars);
+  s.moved = s.xflags + 2 * 4;
+  s.strict = s.moved + 2 * 4;
   s.pids = s.strict + 2;
   return s;
 }
 
 // Per-thread state shared by both token paths.
 struct State {
-  float o[16][4];  // readout accumulators: channel block cb (8 channels), C fragment
+  float o[16][4];  // readout accumulators: 16 blocks of 8 channels, C fragment
   float mterm[2];  // sum_t p_t * min_t for rows g, g+8 (packed path only)
   float m_run;     // reference max of head 4*warp + lane/8 (log2 units), shared by its 8 lanes
   float l_part;    // this lane's share of the running sum (reduced over the 8 lanes at the end)
@@ -182,246 +215,6 @@ __device__ __forceinline__ void load_p(const Shared& sh, int buf, float2 (&pf)[4
   pf[1] = *reinterpret_cast<const float2*>(pb + (g + 8) * kRowStride + 2 * q);
   pf[2] = *reinterpret_cast<const float2*>(pb + g * kRowStride + 8 + 2 * q);
   pf[3] = *reinterpret_cast<const float2*>(pb + (g + 8) * kRowStride + 8 + 2 * q);
-}
-
-// ------------------------------------------------------------------ packed tokens
-template <int BITS>
-__device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int T, int split,
-                             const uint32_t (&qa)[8][4], const float (&qsum)[2], const float (&qr)[8],
-                             State& st, int32_t& flags) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-  const int lo = p.S, hi = T - p.W;
-  int sub_begin = 0, n_my = 0;
-  if (hi > lo) {
-    const int first = lo / kTile, last = (hi - 1) / kTile;
-    const int n_total = last - first + 1;
-    sub_begin = first + static_cast<int>((static_cast<long long>(n_total) * split) / p.n_split);
-    const int sub_end = first + static_cast<int>((static_cast<long long>(n_total) * (split + 1)) / p.n_split);
-    n_my = sub_end - sub_begin;
-  }
-  // validate the page ids this split reads; a bad id drops the split's work
-  {
-    bool bad = false;
-    const int pg0 = (sub_begin * kTile) >> p.p_shift;
-    const int pg1 = n_my > 0 ? (((sub_begin + n_my) * kTile - 1) >> p.p_shift) : pg0 - 1;
-    for (int pg = pg0 + static_cast<int>(threadIdx.x); pg <= pg1; pg += kThreads) {
-      const int32_t pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
-      bad |= pid < 0 || pid >= p.n_pages;
-      if (pg - pg0 < kMaxSplitPages) sh.pids[pg - pg0] = pid;  // refills read ids from here
-    }
-    if (__syncthreads_or(bad)) {
-      flags |= kErrBadPage;
-      n_my = 0;
-    }
-  }
-  if (n_my == 0) return;
-
-  constexpr int kStageBytes = packed_stage_bytes(BITS);
-  constexpr int kLatBytes = kTile * 64 * BITS;
-  const uint8_t* pool = p.pool;
-  // Stage i is filled by four bulk copies, one issued by lane 0 of each warp (the stage's
-  // mbarrier expects four arrivals), so no warp carries the whole producer load.
-  auto issue_part = [&](int i, int part) {
-    const int k = sub_begin + i;
-    const int pg = (k * kTile) >> p.p_shift, tp0 = (k * kTile) & (p.P - 1);
-    const int pg0 = (sub_begin * kTile) >> p.p_shift;
-    const int32_t pid = pg - pg0 < kMaxSplitPages ? sh.pids[pg - pg0]
-                                                 : __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
-    const uint8_t* base = pool + static_cast<size_t>(pid) * static_cast<size_t>(p.page_bytes);
-    uint8_t* dst = sh.stages + (i % kStages) * kStageBytes;
-    uint64_t* bar = sh.bars + (i % kStages);
-    if (part == 0) {
-      mbar_arrive_expect_tx(bar, kLatBytes);
-      bulk_g2s(dst, base + (tp0 / 8) * 4 * (128 * BITS), kLatBytes, bar);
-    } else if (part == 1) {
-      mbar_arrive_expect_tx(bar, 512);
-      bulk_g2s(dst + kLatBytes, base + static_cast<size_t>(p.P) * 64 * BITS + (tp0 / 16) * 512, 512, bar);
-    } else if (part == 2) {
-      mbar_arrive_expect_tx(bar, 256);
-      bulk_g2s(dst + kLatBytes + 512, base + static_cast<size_t>(p.P) * (64 * BITS + 32) + tp0 * 16, 256, bar);
-    } else {
-      mbar_arrive_expect_tx(bar, 256);
-      bulk_g2s(dst + kLatBytes + 768, base + static_cast<size_t>(p.P) * (64 * BITS + 48), 256, bar);
-    }
-  };
-  int issued = 0;  // identical in every thread
-  if (lane == 0)
-    for (int i = 0; i < kStages && i < n_my; ++i) issue_part(i, warp);
-  issued = n_my < kStages ? n_my : kStages;
-
-  // per-page rope factors: query times channel scale split into two BF16 terms
-  uint32_t qr_hi[4], qr_lo[4];
-  float rqs[2] = {0.f, 0.f}, rbias[2] = {0.f, 0.f};
-  int cur_pg = -1;
-
-  for (int i = 0; i < n_my; ++i) {
-    const int stg = i % kStages;
-    const bool ok = mbar_wait_bounded(sh.bars + stg, (i / kStages) & 1, kWaitBudget);
-    const uint8_t* sp = sh.stages + stg * kStageBytes;
-    const int k = sub_begin + i, t0 = k * kTile;
-    const int pg = t0 >> p.p_shift;
-    if (pg != cur_pg) {
-      cur_pg = pg;
-      const uint32_t* rm = reinterpret_cast<const uint32_t*>(sp + kLatBytes + 768) + 16 * warp;
-      // A fragment element (row, dim): dims 2q, 2q+1 (regs 0, 1) and 2q+8, 2q+9 (regs 2, 3)
-      const int dims[4] = {2 * q, 2 * q + 1, 2 * q + 8, 2 * q + 9};
-      float sc[4], mn[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t w = rm[dims[e]];
-        sc[e] = half_lo(w);
-        mn[e] = half_hi(w);
-      }
-      float hi_v[8], lo_v[8];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        rqs[r] = 0.f;
-        rbias[r] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float x = qr[4 * r + e] * sc[e];
-          const float xh = __bfloat162float(__float2bfloat16_rn(x));
-          const float xl = __bfloat162float(__float2bfloat16_rn(x - xh));
-          hi_v[4 * r + e] = xh;
-          lo_v[4 * r + e] = xl;
-          rqs[r] += xh + xl;
-          rbias[r] += qr[4 * r + e] * mn[e];
-        }
-#pragma unroll
-        for (int o = 1; o < 4; o <<= 1) {
-          rqs[r] += __shfl_xor_sync(0xffffffffu, rqs[r], o);
-          rbias[r] += __shfl_xor_sync(0xffffffffu, rbias[r], o);
-        }
-      }
-      // fragment regs: a0 (row g, dims 2q..), a1 (row g+8, dims 2q..), a2 (row g, 2q+8..), a3 (row g+8, 2q+8..)
-      qr_hi[0] = pack_bf16x2(hi_v[0], hi_v[1]);
-      qr_hi[1] = pack_bf16x2(hi_v[4], hi_v[5]);
-      qr_hi[2] = pack_bf16x2(hi_v[2], hi_v[3]);
-      qr_hi[3] = pack_bf16x2(hi_v[6], hi_v[7]);
-      qr_lo[0] = pack_bf16x2(lo_v[0], lo_v[1]);
-      qr_lo[1] = pack_bf16x2(lo_v[4], lo_v[5]);
-      qr_lo[2] = pack_bf16x2(lo_v[2], lo_v[3]);
-      qr_lo[3] = pack_bf16x2(lo_v[6], lo_v[7]);
-    }
-
-    // ---- unpack codes as BF16 integers 128 + n (exact), fragment layout of the page
-    uint32_t bq[2][8][2];  // [n-block][k-chunk][reg]
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
-      const uint8_t* blk = sp + (nb * 4 + warp) * (128 * BITS) + lane * (4 * BITS);
-      if constexpr (BITS == 4) {
-        const uint4 v = *reinterpret_cast<const uint4*>(blk);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int s = 0; s < 4; ++s)
-            bq[nb][2 * j + (s >> 1)][s & 1] = and_or(w4[j] >> (4 * s), 0x000f000fu, 0x43004300u);
-      } else {
-        const uint2 v = *reinterpret_cast<const uint2*>(blk);
-        const uint32_t w2[2] = {v.x, v.y};
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-          for (int s = 0; s < 8; ++s)
-            bq[nb][4 * j + (s >> 1)][s & 1] = and_or(w2[j] >> (2 * s), 0x00030003u, 0x43004300u);
-      }
-    }
-    uint32_t rb[2][2];
-    {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(sp + kLatBytes + warp * 128 + lane * 4);
-#pragma unroll
-      for (int s = 0; s < 4; ++s) rb[s >> 1][s & 1] = and_or(w >> (4 * s), 0x000f000fu, 0x43004300u);
-    }
-
-    // ---- scores on tensor cores
-    // four independent accumulation chains per n-block pair keep the tensor pipe busy
-    float acc[2][4], acc1[2][4], racc[2][4];
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
-      mma_bf16_16816_z(acc[nb], qa[0], bq[nb][0][0], bq[nb][0][1]);
-      mma_bf16_16816_z(acc1[nb], qa[1], bq[nb][1][0], bq[nb][1][1]);
-    }
-#pragma unroll
-    for (int kc = 2; kc < 8; kc += 2)
-#pragma unroll
-      for (int nb = 0; nb < 2; ++nb) {
-        mma_bf16_16816(acc[nb], qa[kc], bq[nb][kc][0], bq[nb][kc][1]);
-        mma_bf16_16816(acc1[nb], qa[kc + 1], bq[nb][kc + 1][0], bq[nb][kc + 1][1]);
-      }
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
-      mma_bf16_16816_z(racc[nb], qr_hi, rb[nb][0], rb[nb][1]);
-      mma_bf16_16816(racc[nb], qr_lo, rb[nb][0], rb[nb][1]);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[nb][e] += acc1[nb][e];
-    }
-    // token metadata: group `warp`, tokens 8nb + 2q + e
-    float tsc[2][2], tmn[2][2];
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int tok = 8 * nb + 2 * q + e;
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(sp + kLatBytes + 512 + (tok * 4 + warp) * 4);
-        tsc[nb][e] = half_lo(w);
-        tmn[nb][e] = half_hi(w);
-      }
-    float part[2][4];
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = e >> 1, c = e & 1;
-        part[nb][e] = tsc[nb][c] * (acc[nb][e] - 128.f * qsum[r]) + tmn[nb][c] * qsum[r] +
-                      (racc[nb][e] - 128.f * rqs[r]) + rbias[r];
-      }
-    // token scales large enough that p * scale could overflow FP16 when p reaches 2^8
-    const int buf = i & 1;
-    if (fmaxf(fmaxf(tsc[0][0], tsc[0][1]), fmaxf(tsc[1][0], tsc[1][1])) >= kStrictScale) sh.strict[buf] = 1;
-
-    // transpose the codes into the readout operand while the exchange is in flight:
-    // 0x4300|n read as FP16 is 3.5 + n/512; subtracting 3.5 leaves n/512 exactly
-#pragma unroll
-    for (int kc = 0; kc < 8; ++kc)
-#pragma unroll
-      for (int r = 0; r < 2; ++r)
-#pragma unroll
-        for (int nb = 0; nb < 2; ++nb) bq[nb][kc][r] = hsub2_u32(movmatrix_t(bq[nb][kc][r]), 0x43004300u);
-
-    if (exchange_partials(sh, buf, part, !ok)) {
-      flags |= kErrTimeout;
-      // orderly exit: bounded waits for the copies still in flight into this CTA
-      if (threadIdx.x == 0)
-        for (int j = i; j < issued; ++j)
-          (void)mbar_wait_bounded(sh.bars + (j % kStages), (j / kStages) & 1, kWaitBudget >> 4);
-      break;
-    }
-    // the previous stage is free once every warp passed the first exchange barrier
-    if (i >= 1 && issued < n_my) {
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        issue_part(issued, warp);
-      }
-      ++issued;
-    }
-    softmax_publish(sh, buf, t0, lo, hi, p.scale_log2, st);
-
-    // ---- readout: A = P * token scale (FP16), B = codes / 512 (FP16, exact)
-    float2 pf[4];
-    load_p(sh, buf, pf);
-    uint32_t a[4];
-    a[0] = pack_f16x2(pf[0].x * tsc[0][0], pf[0].y * tsc[0][1]);
-    a[1] = pack_f16x2(pf[1].x * tsc[0][0], pf[1].y * tsc[0][1]);
-    a[2] = pack_f16x2(pf[2].x * tsc[1][0], pf[2].y * tsc[1][1]);
-    a[3] = pack_f16x2(pf[3].x * tsc[1][0], pf[3].y * tsc[1][1]);
-    st.mterm[0] += pf[0].x * tmn[0][0] + pf[0].y * tmn[0][1] + pf[2].x * tmn[1][0] + pf[2].y * tmn[1][1];
-    st.mterm[1] += pf[1].x * tmn[0][0] + pf[1].y * tmn[0][1] + pf[3].x * tmn[1][0] + pf[3].y * tmn[1][1];
-#pragma unroll
-    for (int kc = 0; kc < 8; ++kc)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) mma_f16_16816(st.o[2 * kc + r], a, bq[0][kc][r], bq[1][kc][r]);
-  }
 }
 
 // ------------------------------------------------------------------ protected (BF16) tokens
@@ -534,31 +327,532 @@ __device__ void bf16_split(const DecodeParams& p, const Shared& sh, int b, int T
   }
 }
 
-template <int BITS>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const DecodeParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const Shared sh = carve<BITS>(smem);
-  const int split = blockIdx.x, hb = blockIdx.y, b = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-  const int h0 = hb * 16;
-  int32_t flags = 0;
+// ------------------------------------------------------------------ packed tokens
+// A matrix load of one 16-byte chunk per token gives lane (g, q) the 16-bit elements 2q, 2q+1
+// of token g (score side) or elements g of tokens 2q, 2q+1 (transposed, readout side). An
+// INT4 element holds 4 channels (nibble s), an INT2 element 8 channels (field i). Masking one
+// nibble/field position of both halves of a register gives an FP16 operand pair whose values
+// are code * 2^-24 * 2^lw; lw = 4s-style weights are folded into the query (scores) and into
+// the output scale (readout).
 
-  int T = __ldg(p.seq_lens + b);
-  if (T < 0 || static_cast<long long>(T) > static_cast<long long>(p.max_pages) * p.P) {
-    flags |= kErrSeqOverflow;
-    T = 0;
+// Channel (within the warp's 128-channel group) of query slot sigma of k-chunk kc, where the
+// slots of lane q are the fragment's k indices 2q, 2q+1, 2q+8, 2q+9.
+template <int BITS>
+__device__ __forceinline__ int slot_channel(int kc, int sigma, int q) {
+  if constexpr (BITS == 4) {
+    // k-chunk 2m + s: mask position s of the words of chunk m (channels 32m + 8q + 0..7);
+    // the pair (low, high half) of position s is (8q + s, 8q + 4 + s), the shifted word gives
+    // (8q + 2 + s, 8q + 6 + s)
+    const int off = sigma == 0 ? 0 : sigma == 1 ? 4 : sigma == 2 ? 2 : 6;
+    return 32 * (kc >> 1) + 8 * q + (kc & 1) + off;
+  } else {
+    // k-chunk 4m + j: fields 2j, 2j+1 of the words of chunk m (channels 64m + 16q + 0..15);
+    // field i of the (low, high) half is channel (16q + i, 16q + 8 + i)
+    const int i = 2 * (kc & 3) + (sigma >> 1);
+    return 64 * (kc >> 2) + 16 * q + 8 * (sigma & 1) + i;
   }
-  if (threadIdx.x == 0) {
-    // packed stages: four arrivals (one copy per warp); protected-token stages: one arrival
-    for (int i = 0; i < kStages; ++i) mbar_init(sh.bars + i, split == p.n_split ? 1 : 4);
-    fence_mbar_init();
-    sh.strict[0] = sh.strict[1] = 0;
+}
+// log2 of the weight the mask leaves on slot sigma of k-chunk kc (equal for both halves of
+// a register).
+template <int BITS>
+__device__ __forceinline__ int slot_log2w(int kc, int sigma) {
+  if constexpr (BITS == 4) {
+    return 4 * (kc & 1);
+  } else {
+    const int i = 2 * (kc & 3) + (sigma >> 1);
+    return 2 * (i <= 4 ? i : i - 5);  // fields 5..7 are masked after a 10-bit shift
+  }
+}
+// Readout block cb, column n: output channel within the group and log2 weight.
+template <int BITS>
+__device__ __forceinline__ int out_channel(int cb, int n) {
+  if constexpr (BITS == 4) return 32 * (cb >> 2) + 4 * n + (cb & 3);
+  else return 64 * (cb >> 3) + 8 * n + (cb & 7);
+}
+template <int BITS>
+__host__ __device__ constexpr int out_log2w(int cb) {
+  return BITS == 4 ? 4 * (cb & 1) : 2 * ((cb & 7) <= 4 ? (cb & 7) : (cb & 7) - 5);
+}
+
+// Largest power-of-two exponent E with max_abs * 2^E < 2^15 (FP16-safe prescale of a query
+// row), kept in [-100, 100]; `range` reports queries too large for the prescale.
+__device__ __forceinline__ int prescale_exponent(float max_abs, bool& range) {
+  if (!(max_abs > 0.f)) return 0;
+  int e = static_cast<int>((__float_as_uint(max_abs) >> 23) & 0xffu) - 127;
+  if (e < -126) e = -126;
+  int E = 14 - e;
+  if (E < -100) {
+    E = -100;
+    range = true;
+  }
+  return E > 100 ? 100 : E;
+}
+
+template <int BITS>
+__device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int T, int split, State& st,
+                             int32_t& flags) {
+  using G = Geom<BITS>;
+  constexpr int kS = G::kStages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const int h0 = blockIdx.y * 16;
+  const int lo = p.S, hi = T - p.W;
+  int tile_begin = 0, n_my = 0;
+  if (hi > lo) {
+    const int first = lo / kPT, last = (hi - 1) / kPT;
+    const int n_total = last - first + 1;
+    tile_begin = first + static_cast<int>((static_cast<long long>(n_total) * split) / p.n_split);
+    const int tile_end = first + static_cast<int>((static_cast<long long>(n_total) * (split + 1)) / p.n_split);
+    n_my = tile_end - tile_begin;
+  }
+  const int pg0 = (tile_begin * kPT) >> p.p_shift;
+  // validate the page ids this split reads; a bad id drops the split's work
+  {
+    bool bad = false;
+    const int pg1 = n_my > 0 ? (((tile_begin + n_my) * kPT - 1) >> p.p_shift) : pg0 - 1;
+    for (int pg = pg0 + static_cast<int>(threadIdx.x); pg <= pg1; pg += kThreads) {
+      const int32_t pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
+      bad |= pid < 0 || pid >= p.n_pages;
+      if (pg - pg0 < kMaxSplitPages) sh.pids[pg - pg0] = pid;  // the copies read ids from here
+    }
+    if (__syncthreads_or(bad)) {
+      flags |= kErrBadPage;
+      n_my = 0;
+    }
+  }
+
+  // Tile i (local index) is one stage: four bulk copies completing on the stage's barrier.
+  auto issue = [&](int i) {
+    const int t0 = (tile_begin + i) * kPT;
+    const int pg = t0 >> p.p_shift, tp0 = t0 & (p.P - 1);
+    const int32_t pid = pg - pg0 < kMaxSplitPages ? sh.pids[pg - pg0]
+                                                 : __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
+    const uint8_t* base = p.pool + static_cast<size_t>(pid) * static_cast<size_t>(p.page_bytes);
+    uint8_t* dst = sh.stages + (i % kS) * G::kStage;
+    uint64_t* bar = sh.bars + (i % kS);
+    const size_t P = static_cast<size_t>(p.P);
+    mbar_arrive_expect_tx(bar, G::kStage);
+    bulk_g2s(dst, base + static_cast<size_t>(tp0) * G::kRowBytes, G::kLat, bar);
+    bulk_g2s(dst + G::kRopeOff, base + P * G::kRowBytes + static_cast<size_t>(tp0 / 16) * 512, 1024, bar);
+    bulk_g2s(dst + G::kMetaOff, base + P * (G::kRowBytes + 32) + static_cast<size_t>(tp0) * 16, 512, bar);
+    bulk_g2s(dst + G::kRMetaOff, base + P * (G::kRowBytes + 48), 256, bar);
+  };
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kS && i < n_my; ++i) issue(i);
+  int issued = n_my < kS ? n_my : kS;  // identical in every thread
+
+  // ---- query operands: FP16 with a per-head power-of-two prescale, in the masks' channel order
+  uint32_t qa[8][4];
+  float qsum[2] = {0.f, 0.f}, f_lat[2];
+  {
+    const uint16_t* r0 = p.q_lat + (static_cast<size_t>(b) * p.H + h0 + g) * kLatent + 128 * warp;
+    const uint16_t* r1 = r0 + 8 * kLatent;
+    float mx0 = 0.f, mx1 = 0.f;
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int c0 = slot_channel<BITS>(kc, 2 * j, q), c1 = slot_channel<BITS>(kc, 2 * j + 1, q);
+        const uint32_t v0 = static_cast<uint32_t>(__ldg(r0 + c0)) | (static_cast<uint32_t>(__ldg(r0 + c1)) << 16);
+        const uint32_t v1 = static_cast<uint32_t>(__ldg(r1 + c0)) | (static_cast<uint32_t>(__ldg(r1 + c1)) << 16);
+        qa[kc][2 * j] = v0;      // a0 / a2: row g
+        qa[kc][2 * j + 1] = v1;  // a1 / a3: row g + 8
+        qsum[0] += bf16_lo(v0) + bf16_hi(v0);
+        qsum[1] += bf16_lo(v1) + bf16_hi(v1);
+        mx0 = fmaxf(mx0, fmaxf(fabsf(bf16_lo(v0)), fabsf(bf16_hi(v0))));
+        mx1 = fmaxf(mx1, fmaxf(fabsf(bf16_lo(v1)), fabsf(bf16_hi(v1))));
+      }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+      qsum[0] += __shfl_xor_sync(0xffffffffu, qsum[0], o);
+      qsum[1] += __shfl_xor_sync(0xffffffffu, qsum[1], o);
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    if (q == 0) {
+      sh.qmax[warp * 16 + g] = mx0;
+      sh.qmax[warp * 16 + g + 8] = mx1;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      mx0 = fmaxf(mx0, sh.qmax[w * 16 + g]);
+      mx1 = fmaxf(mx1, sh.qmax[w * 16 + g + 8]);
+    }
+    bool range = false;
+    const int E0 = prescale_exponent(mx0, range), E1 = prescale_exponent(mx1, range);
+    if (range) flags |= kErrRange;
+    f_lat[0] = pow2i(24 - E0);
+    f_lat[1] = pow2i(24 - E1);
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int lw = slot_log2w<BITS>(kc, 2 * j);
+        const float s0 = pow2i(E0 - lw), s1 = pow2i(E1 - lw);
+        const uint32_t v0 = qa[kc][2 * j], v1 = qa[kc][2 * j + 1];
+        qa[kc][2 * j] = pack_f16x2(bf16_lo(v0) * s0, bf16_hi(v0) * s0);
+        qa[kc][2 * j + 1] = pack_f16x2(bf16_lo(v1) * s1, bf16_hi(v1) * s1);
+      }
+  }
+  // k_R query slice: rows g, g+8, dims 16w + {2q, 2q+1, 2q+8, 2q+9}
+  float qr[8];
+  {
+    const uint32_t* r0 = reinterpret_cast<const uint32_t*>(p.q_rope + (static_cast<size_t>(b) * p.H + h0 + g) * kRope + 16 * warp);
+    const uint32_t* r1 = r0 + 8 * kRope / 2;
+    const uint32_t u0 = __ldg(r0 + q), u1 = __ldg(r1 + q), u2 = __ldg(r0 + 4 + q), u3 = __ldg(r1 + 4 + q);
+    qr[0] = bf16_lo(u0);
+    qr[1] = bf16_hi(u0);
+    qr[2] = bf16_lo(u2);
+    qr[3] = bf16_hi(u2);
+    qr[4] = bf16_lo(u1);
+    qr[5] = bf16_hi(u1);
+    qr[6] = bf16_lo(u3);
+    qr[7] = bf16_hi(u3);
+  }
+  // per-page rope factors: query times channel scale split into two BF16 terms
+  uint32_t qr_hi[4], qr_lo[4];
+  float rconst[2] = {0.f, 0.f};
+  int cur_pg = -1;
+
+  // per-lane matrix-load offsets inside a stage's latent rows (chunk XOR token mod 8)
+  const int r8 = lane & 7, mi = lane >> 3;
+  int off_s, off_r0, off_r1;
+  if constexpr (BITS == 4) {
+    off_s = r8 * 256 + 16 * ((4 * warp + mi) ^ r8);                                  // + 2048 nb
+    off_r0 = (8 * (mi & 1) + r8) * 256 + 16 * ((4 * warp + (mi >> 1)) ^ r8);         // chunks 0, 1
+    off_r1 = (8 * (mi & 1) + r8) * 256 + 16 * ((4 * warp + 2 + (mi >> 1)) ^ r8);     // chunks 2, 3
+  } else {
+    off_s = (8 * (mi >> 1) + r8) * 128 + 16 * ((2 * warp + (mi & 1)) ^ r8);          // + 2048 pair
+    off_r0 = (8 * (mi & 1) + r8) * 128 + 16 * ((2 * warp + (mi >> 1)) ^ r8);
+    off_r1 = off_r0;
+  }
+  uint64_t* const xs_bar = sh.bars + kS;
+  uint64_t* const xp_bar = sh.bars + kS + 2;
+  const float scale_log2 = p.scale_log2;
+
+  // ---- scores of local tile i: partial sums over this warp's channels -> exchange buffer i&1
+  auto score = [&](int i) {
+    const int stg = i % kS, buf = i & 1;
+    const bool ok = mbar_wait_bounded(sh.bars + stg, (i / kS) & 1, kWaitBudget);
+    const uint8_t* sp = sh.stages + stg * G::kStage;
+    const int pg = ((tile_begin + i) * kPT) >> p.p_shift;
+    if (pg != cur_pg) {
+      cur_pg = pg;
+      const uint32_t* rm = reinterpret_cast<const uint32_t*>(sp + G::kRMetaOff) + 16 * warp;
+      // A fragment element (row, dim): dims 2q, 2q+1 (regs 0, 1) and 2q+8, 2q+9 (regs 2, 3)
+      const int dims[4] = {2 * q, 2 * q + 1, 2 * q + 8, 2 * q + 9};
+      float sc[4], mn[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t w = rm[dims[e]];
+        sc[e] = half_lo(w);
+        mn[e] = half_hi(w);
+      }
+      float hi_v[8], lo_v[8], rqs[2], rbias[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        rqs[r] = 0.f;
+        rbias[r] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x = qr[4 * r + e] * sc[e];
+          const float xh = __bfloat162float(__float2bfloat16_rn(x));
+          const float xl = __bfloat162float(__float2bfloat16_rn(x - xh));
+          hi_v[4 * r + e] = xh;
+          lo_v[4 * r + e] = xl;
+          rqs[r] += xh + xl;
+          rbias[r] += qr[4 * r + e] * mn[e];
+        }
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1) {
+          rqs[r] += __shfl_xor_sync(0xffffffffu, rqs[r], o);
+          rbias[r] += __shfl_xor_sync(0xffffffffu, rbias[r], o);
+        }
+        rconst[r] = rbias[r] - 128.f * rqs[r];
+      }
+      qr_hi[0] = pack_bf16x2(hi_v[0], hi_v[1]);
+      qr_hi[1] = pack_bf16x2(hi_v[4], hi_v[5]);
+      qr_hi[2] = pack_bf16x2(hi_v[2], hi_v[3]);
+      qr_hi[3] = pack_bf16x2(hi_v[6], hi_v[7]);
+      qr_lo[0] = pack_bf16x2(lo_v[0], lo_v[1]);
+      qr_lo[1] = pack_bf16x2(lo_v[4], lo_v[5]);
+      qr_lo[2] = pack_bf16x2(lo_v[2], lo_v[3]);
+      qr_lo[3] = pack_bf16x2(lo_v[6], lo_v[7]);
+    }
+
+    // latent: four n-blocks of 8 tokens, eight k-chunks each (four independent chains)
+    float acc[4][4];
+    if constexpr (BITS == 4) {
+      uint32_t R[4][4];
+#pragma unroll
+      for (int nb = 0; nb < 4; ++nb) ldsm_x4(R[nb], sp + nb * 2048 + off_s);
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int nb = 0; nb < 4; ++nb) {
+          const uint32_t x = R[nb][m], x8 = x >> 8;
+          if (m == 0) mma_f16_16816_z(acc[nb], qa[0], x & 0x000f000fu, x8 & 0x000f000fu);
+          else mma_f16_16816(acc[nb], qa[2 * m], x & 0x000f000fu, x8 & 0x000f000fu);
+          mma_f16_16816(acc[nb], qa[2 * m + 1], x & 0x00f000f0u, x8 & 0x00f000f0u);
+        }
+    } else {
+      uint32_t R[4][2];
+#pragma unroll
+      for (int pp = 0; pp < 2; ++pp) {
+        uint32_t X[4];
+        ldsm_x4(X, sp + pp * 2048 + off_s);
+        R[2 * pp][0] = X[0];
+        R[2 * pp][1] = X[1];
+        R[2 * pp + 1][0] = X[2];
+        R[2 * pp + 1][1] = X[3];
+      }
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int nb = 0; nb < 4; ++nb) {
+          const uint32_t x = R[nb][m], xs = x >> 10;
+          uint32_t u[8];
+#pragma unroll
+          for (int f = 0; f < 5; ++f) u[f] = x & (0x00030003u << (2 * f));
+#pragma unroll
+          for (int f = 5; f < 8; ++f) u[f] = xs & (0x00030003u << (2 * (f - 5)));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (m == 0 && j == 0) mma_f16_16816_z(acc[nb], qa[0], u[0], u[1]);
+            else mma_f16_16816(acc[nb], qa[4 * m + j], u[2 * j], u[2 * j + 1]);
+          }
+        }
+    }
+    // k_R chunk `warp`: two 16-token blocks, BF16 integers 128 + code (exact)
+    float racc[4][4];
+#pragma unroll
+    for (int tb = 0; tb < 2; ++tb) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(sp + G::kRopeOff + (tb * 4 + warp) * 128 + lane * 4);
+#pragma unroll
+      for (int hb2 = 0; hb2 < 2; ++hb2) {
+        const uint32_t b0 = and_or(w >> (8 * hb2), 0x000f000fu, 0x43004300u);
+        const uint32_t b1 = and_or(w >> (8 * hb2 + 4), 0x000f000fu, 0x43004300u);
+        mma_bf16_16816_z(racc[2 * tb + hb2], qr_hi, b0, b1);
+        mma_bf16_16816(racc[2 * tb + hb2], qr_lo, b0, b1);
+      }
+    }
+    // token metadata of group `warp`: tokens 8nb + 2q + c
+    float* my = sh.sbuf + (buf * 4 + warp) * 16 * kXStride;
+    bool big = false;
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb) {
+      float tsc[2], tmn[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int tok = 8 * nb + 2 * q + c;
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(sp + G::kMetaOff + (tok * 4 + warp) * 4);
+        tsc[c] = half_lo(w);
+        tmn[c] = half_hi(w);
+        big |= tsc[c] >= kStrictScale;
+      }
+      float part[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = e >> 1, c = e & 1;
+        part[e] = fmaf(tsc[c] * f_lat[r], acc[nb][e], racc[nb][e] + fmaf(tmn[c], qsum[r], rconst[r]));
+      }
+      *reinterpret_cast<float2*>(my + g * kXStride + 8 * nb + 2 * q) = make_float2(part[0], part[1]);
+      *reinterpret_cast<float2*>(my + (g + 8) * kXStride + 8 * nb + 2 * q) = make_float2(part[2], part[3]);
+    }
+    big = __any_sync(0xffffffffu, big);
+    if (lane == 0) sh.xflags[buf * 4 + warp] = (big ? 1 : 0) | (ok ? 0 : 2);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(xs_bar + buf);
+  };
+
+  // ---- online softmax of tile i: heads 4w..4w+3, lane -> head 4w + lane/8, tokens 4*(lane%8)..+3
+  auto softmax = [&](int i, bool strict) -> bool {
+    const int buf = i & 1;
+    const int hh = 4 * warp + (lane >> 3), tt = 4 * (lane & 7);
+    const int t0 = (tile_begin + i) * kPT;
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float4 v = *reinterpret_cast<const float4*>(sh.sbuf + ((buf * 4 + w) * 16 + hh) * kXStride + tt);
+      s[0] += v.x;
+      s[1] += v.y;
+      s[2] += v.z;
+      s[3] += v.w;
+    }
+    float lmax = -INFINITY;
+    bool valid[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      valid[j] = (t0 + tt + j >= lo) && (t0 + tt + j < hi);
+      s[j] = valid[j] ? s[j] * scale_log2 : -INFINITY;
+      lmax = fmaxf(lmax, s[j]);
+    }
+    const float slack = strict ? 0.f : kRescaleSlack;
+    const bool need = lmax > st.m_run + slack || (st.m_run == -INFINITY && lmax > -INFINITY);
+    float alpha = 1.f;
+    const bool moved = __any_sync(0xffffffffu, need);
+    if (moved) {  // rare: some head of this warp needs a new reference max
+      float tmax = lmax;
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+      if (tmax > st.m_run + slack || (st.m_run == -INFINITY && tmax > -INFINITY)) {
+        alpha = exp2f(st.m_run - tmax);  // 0 when the old reference was -inf
+        st.l_part *= alpha;
+        st.m_run = tmax;
+      }
+    }
+    float pv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pv[j] = (valid[j] && st.m_run != -INFINITY) ? exp2f(s[j] - st.m_run) : 0.f;
+    st.l_part += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+    *reinterpret_cast<float4*>(sh.pbuf + (buf * 16 + hh) * kXStride + tt) = make_float4(pv[0], pv[1], pv[2], pv[3]);
+    if ((lane & 7) == 0) sh.alpha[buf * 16 + hh] = alpha;
+    if (lane == 0) sh.moved[buf * 4 + warp] = moved ? 1 : 0;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(xp_bar + buf);
+    return moved;
+  };
+
+  // ---- readout of tile i: O += (P * token scale) . codes, plus sum_t P * token min
+  auto readout = [&](int i) {
+    const int stg = i % kS, buf = i & 1;
+    const uint8_t* sp = sh.stages + stg * G::kStage;
+    const float* pb = sh.pbuf + buf * 16 * kXStride;
+#pragma unroll
+    for (int kc2 = 0; kc2 < 2; ++kc2) {
+      // P fragment: rows g, g+8; tokens 16kc2 + 2q + {0, 1} (regs 0, 1) and + 8 (regs 2, 3)
+      const int ta = 16 * kc2 + 2 * q, tb = ta + 8;
+      const float2 p0 = *reinterpret_cast<const float2*>(pb + g * kXStride + ta);
+      const float2 p1 = *reinterpret_cast<const float2*>(pb + (g + 8) * kXStride + ta);
+      const float2 p2 = *reinterpret_cast<const float2*>(pb + g * kXStride + tb);
+      const float2 p3 = *reinterpret_cast<const float2*>(pb + (g + 8) * kXStride + tb);
+      const uint32_t wa0 = *reinterpret_cast<const uint32_t*>(sp + G::kMetaOff + (ta * 4 + warp) * 4);
+      const uint32_t wa1 = *reinterpret_cast<const uint32_t*>(sp + G::kMetaOff + ((ta + 1) * 4 + warp) * 4);
+      const uint32_t wb0 = *reinterpret_cast<const uint32_t*>(sp + G::kMetaOff + (tb * 4 + warp) * 4);
+      const uint32_t wb1 = *reinterpret_cast<const uint32_t*>(sp + G::kMetaOff + ((tb + 1) * 4 + warp) * 4);
+      const float sa0 = half_lo(wa0), sa1 = half_lo(wa1), sb0 = half_lo(wb0), sb1 = half_lo(wb1);
+      uint32_t a[4];
+      a[0] = pack_f16x2(p0.x * sa0, p0.y * sa1);
+      a[1] = pack_f16x2(p1.x * sa0, p1.y * sa1);
+      a[2] = pack_f16x2(p2.x * sb0, p2.y * sb1);
+      a[3] = pack_f16x2(p3.x * sb0, p3.y * sb1);
+      const float ma0 = half_hi(wa0), ma1 = half_hi(wa1), mb0 = half_hi(wb0), mb1 = half_hi(wb1);
+      st.mterm[0] += (p0.x * ma0 + p0.y * ma1) + (p2.x * mb0 + p2.y * mb1);
+      st.mterm[1] += (p1.x * ma0 + p1.y * ma1) + (p3.x * mb0 + p3.y * mb1);
+      if constexpr (BITS == 4) {
+#pragma unroll
+        for (int mp = 0; mp < 2; ++mp) {
+          uint32_t X[4];  // (tokens 0-7, chunk 2mp), (8-15, 2mp), (0-7, 2mp+1), (8-15, 2mp+1)
+          ldsm_x4_t(X, sp + kc2 * 16 * 256 + (mp == 0 ? off_r0 : off_r1));
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int mm = 2 * mp + hf;
+            const uint32_t x0 = X[2 * hf], x1 = X[2 * hf + 1], y0 = x0 >> 8, y1 = x1 >> 8;
+            mma_f16_16816(st.o[4 * mm + 0], a, x0 & 0x000f000fu, x1 & 0x000f000fu);
+            mma_f16_16816(st.o[4 * mm + 1], a, x0 & 0x00f000f0u, x1 & 0x00f000f0u);
+            mma_f16_16816(st.o[4 * mm + 2], a, y0 & 0x000f000fu, y1 & 0x000f000fu);
+            mma_f16_16816(st.o[4 * mm + 3], a, y0 & 0x00f000f0u, y1 & 0x00f000f0u);
+          }
+        }
+      } else {
+        uint32_t X[4];  // (tokens 0-7, chunk 0), (8-15, 0), (0-7, 1), (8-15, 1)
+        ldsm_x4_t(X, sp + kc2 * 16 * 128 + off_r0);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const uint32_t x0 = X[2 * m], x1 = X[2 * m + 1], y0 = x0 >> 10, y1 = x1 >> 10;
+#pragma unroll
+          for (int f = 0; f < 5; ++f)
+            mma_f16_16816(st.o[8 * m + f], a, x0 & (0x00030003u << (2 * f)), x1 & (0x00030003u << (2 * f)));
+#pragma unroll
+          for (int f = 5; f < 8; ++f)
+            mma_f16_16816(st.o[8 * m + f], a, y0 & (0x00030003u << (2 * (f - 5))), y1 & (0x00030003u << (2 * (f - 5))));
+        }
+      }
+    }
+  };
+
+  // ---- pipeline: scores of tile i+1 overlap the softmax exchange of tile i
+  if (n_my > 0) score(0);
+  for (int i = 0; i < n_my; ++i) {
+    const int buf = i & 1;
+    const uint32_t par = (i >> 1) & 1;
+    bool ok = mbar_wait_bounded(xs_bar + buf, par, kWaitBudget);
+    const int xf = sh.xflags[buf * 4] | sh.xflags[buf * 4 + 1] | sh.xflags[buf * 4 + 2] | sh.xflags[buf * 4 + 3];
+    if (!ok || (xf & 2)) {
+      flags |= kErrTimeout;
+      if (threadIdx.x == 0)  // orderly exit: bounded waits for the copies still in flight
+        for (int j = i + 1; j < issued; ++j)
+          (void)mbar_wait_bounded(sh.bars + (j % kS), (j / kS) & 1, kWaitBudget >> 4);
+      break;
+    }
+    softmax(i, (xf & 1) != 0);
+    if (i + 1 < n_my) score(i + 1);
+    ok = mbar_wait_bounded(xp_bar + buf, par, kWaitBudget);
+    if (!ok) {
+      flags |= kErrTimeout;
+      if (threadIdx.x == 0)
+        for (int j = i + 1; j < issued; ++j)
+          (void)mbar_wait_bounded(sh.bars + (j % kS), (j / kS) & 1, kWaitBudget >> 4);
+      break;
+    }
+    // every warp finished tile i-1 (its readout precedes the weights of tile i): refill its stage
+    if (i >= 1 && issued < n_my) {
+      if (warp == (i & 3) && lane == 0) {
+        fence_proxy_async_smem();
+        issue(issued);
+      }
+      ++issued;
+    }
+    if (sh.moved[buf * 4] | sh.moved[buf * 4 + 1] | sh.moved[buf * 4 + 2] | sh.moved[buf * 4 + 3]) {
+      const float a0 = sh.alpha[buf * 16 + g], a1 = sh.alpha[buf * 16 + g + 8];
+#pragma unroll
+      for (int cb = 0; cb < 16; ++cb) {
+        st.o[cb][0] *= a0;
+        st.o[cb][1] *= a0;
+        st.o[cb][2] *= a1;
+        st.o[cb][3] *= a1;
+      }
+      st.mterm[0] *= a0;
+      st.mterm[1] *= a1;
+    }
+    readout(i);
+  }
+
+  // ---- partial output: undo the operand weights, add sum_t p_t min_t, store through a
+  // shared-memory tile (the stages are free once every warp is here) for coalesced writes
+  float mt0 = st.mterm[0], mt1 = st.mterm[1];
+#pragma unroll
+  for (int o = 1; o < 4; o <<= 1) {
+    mt0 += __shfl_xor_sync(0xffffffffu, mt0, o);
+    mt1 += __shfl_xor_sync(0xffffffffu, mt1, o);
   }
   __syncthreads();
+  float* tile = reinterpret_cast<float*>(sh.stages);
+#pragma unroll
+  for (int cb = 0; cb < 16; ++cb) {
+    const float sc = pow2i(24 - out_log2w<BITS>(cb));
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int ch = 128 * warp + out_channel<BITS>(cb, 2 * q + c);
+      tile[g * kOutStride + ch] = fmaf(st.o[cb][c], sc, mt0);
+      tile[(g + 8) * kOutStride + ch] = fmaf(st.o[cb][2 + c], sc, mt1);
+    }
+  }
+  __syncthreads();
+  const int NS = p.n_split + 1;
+  for (int idx = threadIdx.x; idx < 16 * (kLatent / 4); idx += kThreads) {
+    const int row = idx / (kLatent / 4), c4 = idx % (kLatent / 4);
+    const float4 v = *reinterpret_cast<const float4*>(tile + row * kOutStride + 4 * c4);
+    *reinterpret_cast<float4*>(p.o_part + ((static_cast<size_t>(b) * p.H + h0 + row) * NS + split) * kLatent + 4 * c4) = v;
+  }
+}
 
-  // query fragments for latent group `warp` (BF16, exact) and their per-row sums
+// ------------------------------------------------------------------ protected-token CTA
+__device__ void protected_split(const DecodeParams& p, const Shared& sh, int b, int T, State& st, int32_t& flags) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const int h0 = blockIdx.y * 16;
+  // query fragments for latent group `warp` (BF16, exact, channels in order)
   uint32_t qa[8][4];
-  float qsum[2] = {0.f, 0.f};
   {
     const uint32_t* r0 = reinterpret_cast<const uint32_t*>(p.q_lat + (static_cast<size_t>(b) * p.H + h0 + g) * kLatent + 128 * warp);
     const uint32_t* r1 = r0 + 8 * kLatent / 2;
@@ -568,18 +862,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
       qa[kc][1] = __ldg(r1 + 8 * kc + q);
       qa[kc][2] = __ldg(r0 + 8 * kc + 4 + q);
       qa[kc][3] = __ldg(r1 + 8 * kc + 4 + q);
-      qsum[0] += bf16_lo(qa[kc][0]) + bf16_hi(qa[kc][0]) + bf16_lo(qa[kc][2]) + bf16_hi(qa[kc][2]);
-      qsum[1] += bf16_lo(qa[kc][1]) + bf16_hi(qa[kc][1]) + bf16_lo(qa[kc][3]) + bf16_hi(qa[kc][3]);
-    }
-#pragma unroll
-    for (int o = 1; o < 4; o <<= 1) {
-      qsum[0] += __shfl_xor_sync(0xffffffffu, qsum[0], o);
-      qsum[1] += __shfl_xor_sync(0xffffffffu, qsum[1], o);
     }
   }
   // k_R query slice: rows g, g+8, dims 16w + {2q, 2q+1, 2q+8, 2q+9}
   uint32_t qra[4];
-  float qr[8];
   {
     const uint32_t* r0 = reinterpret_cast<const uint32_t*>(p.q_rope + (static_cast<size_t>(b) * p.H + h0 + g) * kRope + 16 * warp);
     const uint32_t* r1 = r0 + 8 * kRope / 2;
@@ -587,15 +873,46 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
     qra[1] = __ldg(r1 + q);
     qra[2] = __ldg(r0 + 4 + q);
     qra[3] = __ldg(r1 + 4 + q);
-    qr[0] = bf16_lo(qra[0]);
-    qr[1] = bf16_hi(qra[0]);
-    qr[2] = bf16_lo(qra[2]);
-    qr[3] = bf16_hi(qra[2]);
-    qr[4] = bf16_lo(qra[1]);
-    qr[5] = bf16_hi(qra[1]);
-    qr[6] = bf16_lo(qra[3]);
-    qr[7] = bf16_hi(qra[3]);
   }
+  bf16_split(p, sh, b, T, qa, qra, st, flags);
+
+  const int NS = p.n_split + 1;
+  float* o0 = p.o_part + ((static_cast<size_t>(b) * p.H + h0 + g) * NS + p.n_split) * kLatent + 128 * warp;
+  float* o1 = p.o_part + ((static_cast<size_t>(b) * p.H + h0 + g + 8) * NS + p.n_split) * kLatent + 128 * warp;
+#pragma unroll
+  for (int cb = 0; cb < 16; ++cb) {
+    *reinterpret_cast<float2*>(o0 + 8 * cb + 2 * q) = make_float2(st.o[cb][0], st.o[cb][1]);
+    *reinterpret_cast<float2*>(o1 + 8 * cb + 2 * q) = make_float2(st.o[cb][2], st.o[cb][3]);
+  }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const Shared sh = carve<BITS>(smem);
+  const int split = blockIdx.x, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h0 = blockIdx.y * 16;
+  const bool is_bf16 = split == p.n_split;
+  int32_t flags = 0;
+
+  int T = __ldg(p.seq_lens + b);
+  if (T < 0 || static_cast<long long>(T) > static_cast<long long>(p.max_pages) * p.P) {
+    flags |= kErrSeqOverflow;
+    T = 0;
+  }
+  if (threadIdx.x == 0) {
+    if (is_bf16) {  // two row stages, one arrival each
+      mbar_init(sh.bars, 1);
+      mbar_init(sh.bars + 1, 1);
+    } else {  // packed stages (one arrival + bytes), then the exchanges (one arrival per warp)
+      for (int i = 0; i < Geom<BITS>::kStages; ++i) mbar_init(sh.bars + i, 1);
+      for (int i = 0; i < 4; ++i) mbar_init(sh.bars + Geom<BITS>::kStages + i, 4);
+    }
+    fence_mbar_init();
+    sh.strict[0] = sh.strict[1] = 0;
+  }
+  __syncthreads();
 
   State st;
 #pragma unroll
@@ -604,28 +921,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
   st.m_run = -INFINITY;
   st.l_part = 0.f;
 
-  const bool is_bf16 = split == p.n_split;
-  if (is_bf16) bf16_split(p, sh, b, T, qa, qra, st, flags);
-  else packed_split<BITS>(p, sh, b, T, split, qa, qsum, qr, st, flags);
+  if (is_bf16) protected_split(p, sh, b, T, st, flags);
+  else packed_split<BITS>(p, sh, b, T, split, st, flags);
 
-  // ---- partial results
   const int NS = p.n_split + 1;
-  float mt0 = st.mterm[0], mt1 = st.mterm[1];
-#pragma unroll
-  for (int o = 1; o < 4; o <<= 1) {
-    mt0 += __shfl_xor_sync(0xffffffffu, mt0, o);
-    mt1 += __shfl_xor_sync(0xffffffffu, mt1, o);
-  }
-  const float oscale = is_bf16 ? 1.f : 512.f;
-  float* o0 = p.o_part + ((static_cast<size_t>(b) * p.H + h0 + g) * NS + split) * kLatent + 128 * warp;
-  float* o1 = p.o_part + ((static_cast<size_t>(b) * p.H + h0 + g + 8) * NS + split) * kLatent + 128 * warp;
-#pragma unroll
-  for (int cb = 0; cb < 16; ++cb) {
-    *reinterpret_cast<float2*>(o0 + 8 * cb + 2 * q) =
-        make_float2(oscale * st.o[cb][0] + mt0, oscale * st.o[cb][1] + mt0);
-    *reinterpret_cast<float2*>(o1 + 8 * cb + 2 * q) =
-        make_float2(oscale * st.o[cb][2] + mt1, oscale * st.o[cb][3] + mt1);
-  }
   float l_run = st.l_part;
 #pragma unroll
   for (int o = 1; o < 8; o <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, o);
@@ -685,7 +984,7 @@ int decode_num_splits(int B, int H, int max_pages, int P, int num_sms) {
   const int groups = B * (H / 16);
   const int target = kCtasPerSm * num_sms;  // one full wave of resident CTAs
   int ns = target / (groups > 0 ? groups : 1) - 1;
-  const long long max_sub = (static_cast<long long>(max_pages) * P) / kTile;
+  const long long max_sub = (static_cast<long long>(max_pages) * P) / kPT;
   int cap = static_cast<int>(max_sub / 4);
   if (cap < 1) cap = 1;
   if (ns > cap) ns = cap;
@@ -709,7 +1008,7 @@ cudaError_t ensure_smem_attr() {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!done[dev]) {
-    e = cudaFuncSetAttribute(decode_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(BITS));
+    e = cudaFuncSetAttribute(decode_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<BITS>());
     if (e != cudaSuccess) return e;
     done[dev] = true;
   }
@@ -721,10 +1020,10 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   cudaError_t e;
   if (p.bits_c == 4) {
     if ((e = ensure_smem_attr<4>()) != cudaSuccess) return e;
-    decode_kernel<4><<<grid, kThreads, smem_bytes(4), stream>>>(p);
+    decode_kernel<4><<<grid, kThreads, smem_bytes<4>(), stream>>>(p);
   } else {
     if ((e = ensure_smem_attr<2>()) != cudaSuccess) return e;
-    decode_kernel<2><<<grid, kThreads, smem_bytes(2), stream>>>(p);
+    decode_kernel<2><<<grid, kThreads, smem_bytes<2>(), stream>>>(p);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -756,3 +1055,4 @@ cudaError_t noalloc_scratch(void** out) {
 }
 
 }  // namespace mlaq
+

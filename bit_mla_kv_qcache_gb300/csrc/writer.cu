@@ -202,40 +202,28 @@ __device__ void write_token(const WriteParams& p, int r, int (&s_cnt)[2][4]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) code[i] = quant_code(x[i], qp.m, qp.s, qp.inv_s, L);
 
-  // ---- pack into the documented fragment layout (region A). This lane holds chunk k = lane/4
-  // (16 channels), positions e = 4m + i of it (m = lane%4): it feeds the words of lanes
-  // q = 2(m%2) + d (d = 0: e = 4m, 4m+1; d = 1: e = 4m+2, 4m+3), h = m/2.
-  const int k = lane >> 2, m = lane & 3, h = m >> 1;
-  uint8_t* blk = page + static_cast<size_t>(((tp >> 3) * 4 + warp) * (128 * p.bits_c));
-  const int lane_base = 4 * (tp & 7);
+  // ---- pack into region A: the token's row keeps its channels in order (this lane's four
+  // channels form 16 bits (INT4) or 8 bits (INT2) at row byte (128w + 4 lane) * bits_c / 8),
+  // and the row's 16-byte chunks are stored XOR-permuted by tp mod 8. Neighbouring lanes
+  // merge into one 32-bit store.
+  uint8_t* row = page + static_cast<size_t>(tp) * (64 * p.bits_c);
+  const int swz = tp & 7;
   if (p.bits_c == 4) {
-    const int sft = 2 * (k & 1) + h;
-    uint32_t w0 = (static_cast<uint32_t>(code[0]) << (4 * sft)) | (static_cast<uint32_t>(code[1]) << (4 * (sft + 4)));
-    uint32_t w1 = (static_cast<uint32_t>(code[2]) << (4 * sft)) | (static_cast<uint32_t>(code[3]) << (4 * (sft + 4)));
-    // a word gathers chunks 2j, 2j+1 and h = 0, 1: lanes differing in bits 1 and 2
-    w0 |= __shfl_xor_sync(0xffffffffu, w0, 2);
-    w1 |= __shfl_xor_sync(0xffffffffu, w1, 2);
-    w0 |= __shfl_xor_sync(0xffffffffu, w0, 4);
-    w1 |= __shfl_xor_sync(0xffffffffu, w1, 4);
-    if ((lane & 6) == 0) {
-      const int q0 = 2 * (m & 1), j = k >> 1;
-      *reinterpret_cast<uint32_t*>(blk + (lane_base + q0) * 16 + j * 4) = w0;
-      *reinterpret_cast<uint32_t*>(blk + (lane_base + q0 + 1) * 16 + j * 4) = w1;
+    uint32_t v = static_cast<uint32_t>(code[0]) | (static_cast<uint32_t>(code[1]) << 4) |
+                 (static_cast<uint32_t>(code[2]) << 8) | (static_cast<uint32_t>(code[3]) << 12);
+    v |= __shfl_down_sync(0xffffffffu, v, 1) << 16;
+    if ((lane & 1) == 0) {
+      const int chunk = 4 * warp + (lane >> 3);  // logical chunk of row byte 64w + 2 lane
+      *reinterpret_cast<uint32_t*>(row + 16 * (chunk ^ swz) + 2 * (lane & 7)) = v;
     }
   } else {
-    const int sft = 2 * (k & 3) + h;
-    uint32_t w0 = (static_cast<uint32_t>(code[0]) << (2 * sft)) | (static_cast<uint32_t>(code[1]) << (2 * (sft + 8)));
-    uint32_t w1 = (static_cast<uint32_t>(code[2]) << (2 * sft)) | (static_cast<uint32_t>(code[3]) << (2 * (sft + 8)));
-    // a word gathers chunks 4j..4j+3 and h = 0, 1: lanes differing in bits 1, 2 and 3
-#pragma unroll
-    for (int o = 2; o <= 8; o <<= 1) {
-      w0 |= __shfl_xor_sync(0xffffffffu, w0, o);
-      w1 |= __shfl_xor_sync(0xffffffffu, w1, o);
-    }
-    if ((lane & 14) == 0) {
-      const int q0 = 2 * (m & 1), j = k >> 2;
-      *reinterpret_cast<uint32_t*>(blk + (lane_base + q0) * 8 + j * 4) = w0;
-      *reinterpret_cast<uint32_t*>(blk + (lane_base + q0 + 1) * 8 + j * 4) = w1;
+    uint32_t v = static_cast<uint32_t>(code[0]) | (static_cast<uint32_t>(code[1]) << 2) |
+                 (static_cast<uint32_t>(code[2]) << 4) | (static_cast<uint32_t>(code[3]) << 6);
+    v |= __shfl_down_sync(0xffffffffu, v, 1) << 8;
+    v |= __shfl_down_sync(0xffffffffu, v, 2) << 16;
+    if ((lane & 3) == 0) {
+      const int chunk = 2 * warp + (lane >> 4);  // logical chunk of row byte 32w + lane
+      *reinterpret_cast<uint32_t*>(row + 16 * (chunk ^ swz) + (lane & 15)) = v;
     }
   }
   // ---- latent metadata (region C)

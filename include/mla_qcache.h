@@ -72,7 +72,8 @@ extern "C" {
  * Cache configuration.
  *   bits_c     latent code width: 4 (C4) or 2 (C2). 2^bits_c levels, L = 2^bits_c - 1.
  *   bits_r     k_R code width: must be 4 (R4).
- *   page_size  P, tokens per cache page: 16, 32, 64 or 128, and P <= n_recent.
+ *   page_size  P, tokens per cache page: 32, 64 or 128, and P <= n_recent (the pages use 64
+ *              and 128; decode streams 32-token tiles that never straddle a page).
  *   n_sink     S, leading tokens kept in BF16 ("sink4"): 0..16.
  *   n_recent   W, trailing tokens kept in BF16 ("local128"): P..1024.
  *   clip_q     per-token clip quantile of |c| for the latent, in (0, 1]; 0 disables the clip.
@@ -107,15 +108,15 @@ typedef struct {
  * its page (position mod P), c a latent channel (0..511), j a k_R channel (0..63).
  *
  *   Region A, latent codes, offset 0, size P*64*bits_c bytes.
- *     Blocks of 8 tokens x 128 channels (one group g = c/128): block (t/8, g) starts at
- *     ((t/8)*4 + g) * 128*bits_c. A block is 32 lanes of 4*bits_c bytes, lane = 4*(t%8) + q,
- *     each lane a run of bits_c little-endian 32-bit words. With cc = c%128,
- *     k = cc/16, e = cc%16, q = (e%8)/2, h = e/8, o = e%2:
- *       bits_c == 4: word k/2, field s = 2*(k%2) + h, bits [4*(s+4*o), 4*(s+4*o)+4)
- *       bits_c == 2: word k/4, field s = 2*(k%4) + h, bits [2*(s+8*o), 2*(s+8*o)+2)
- *     (So shifting a word right by 4*s (or 2*s) and masking the low field of each 16-bit
- *     half yields channels (2q, 2q+1) or (2q+8, 2q+9) of one 16-channel chunk of token t%8:
- *     the B operand of a 16x8x16 tensor-core product with tokens as columns.)
+ *     One row of R = 64*bits_c bytes per token, row t at t*R. Inside a row the channels are
+ *     in order: byte k holds channels 2k (low nibble) and 2k+1 (high nibble) for bits_c == 4,
+ *     channels 4k+i at bits [2i, 2i+2) for bits_c == 2. The row's 16-byte chunks are stored
+ *     XOR-permuted: logical chunk k/16 sits at chunk (k/16) ^ (t%8), i.e. byte
+ *     t*R + 16*((k/16) ^ (t%8)) + k%16.
+ *     (So eight consecutive tokens' copies of one logical chunk fall on eight distinct
+ *     16-byte bank groups: an 8x8 matrix load of 16-bit elements, one row per token, reads
+ *     them without bank conflicts, plain or transposed. Element e of logical chunk j holds
+ *     channels 32j + 4e + s at bits 4s (INT4) or 64j + 8e + i at bits 2i (INT2).)
  *   Region B, k_R codes (4 bits), offset P*64*bits_c, size 32*P bytes.
  *     Blocks of 16 tokens x 16 channels: block (t/16, j/16) starts at ((t/16)*4 + j/16)*128.
  *     A block is 32 lanes of one 32-bit word, lane = 4*(t%8) + q. With e = j%16,

@@ -219,26 +219,16 @@ size_t oracle_page_bytes(const oracle_config* cfg) {
   return P * (64u * (size_t)cfg->bits_c + 32u + 16u) + 256u;
 }
 
-/* Position of latent code (token t of the page, channel c): byte offset in the page and bit shift. */
+/* Position of latent code (token t of the page, channel c): byte offset in the page and bit shift.
+   Region A holds one row of 64*bits_c bytes per token. Byte k of the row carries channels in
+   order (c = 2k low nibble, 2k+1 high nibble for INT4; c = 4k+i at bits 2i for INT2); the
+   row's 16-byte chunks are stored permuted, logical chunk k/16 at chunk (k/16) XOR (t mod 8). */
 void oracle_latent_code_pos(int bits_c, int t, int c, size_t* byte, int* shift) {
-  int g = c / GROUP, cc = c % GROUP;
-  int k = cc / 16, e = cc % 16, q = (e % 8) / 2, h = e / 8, o = e % 2;
-  int lane = 4 * (t % 8) + q;
-  size_t block = ((size_t)(t / 8) * 4 + (size_t)g) * (size_t)(128 * bits_c);
-  size_t lane_off = (size_t)lane * (size_t)(4 * bits_c);
-  int word, pos, width;
-  if (bits_c == 4) {
-    word = k / 2;
-    pos = (2 * (k % 2) + h) + 4 * o;
-    width = 4;
-  } else {
-    word = k / 4;
-    pos = (2 * (k % 4) + h) + 8 * o;
-    width = 2;
-  }
-  int bit = width * pos; /* bit index within the little-endian 32-bit word */
-  *byte = block + lane_off + (size_t)word * 4 + (size_t)(bit / 8);
-  *shift = bit % 8;
+  int row = 64 * bits_c;
+  int k = c * bits_c / 8;
+  int chunk = (k / 16) ^ (t % 8);
+  *byte = (size_t)t * (size_t)row + (size_t)chunk * 16u + (size_t)(k % 16);
+  *shift = (c * bits_c) % 8;
 }
 
 /* Position of k_R code (token t of the page, channel j). */

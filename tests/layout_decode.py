@@ -14,18 +14,10 @@ def latent_positions(bits_c, P):
     """(byte, shift) arrays of shape [P, 512] for every latent code of a page."""
     t = np.arange(P)[:, None]
     c = np.arange(512)[None, :]
-    g, cc = c // 128, c % 128
-    k, e = cc // 16, cc % 16
-    q, h, o = (e % 8) // 2, e // 8, e % 2
-    lane = 4 * (t % 8) + q
-    block = ((t // 8) * 4 + g) * (128 * bits_c)
-    if bits_c == 4:
-        word, pos, width = k // 2, 2 * (k % 2) + h + 4 * o, 4
-    else:
-        word, pos, width = k // 4, 2 * (k % 4) + h + 8 * o, 2
-    bit = width * pos
-    byte = block + lane * (4 * bits_c) + word * 4 + bit // 8
-    return np.broadcast_to(byte, (P, 512)), np.broadcast_to(bit % 8, (P, 512))
+    k = c * bits_c // 8                      # byte of the token's row, channels in order
+    byte = t * (64 * bits_c) + 16 * ((k // 16) ^ (t % 8)) + k % 16
+    shift = (c * bits_c) % 8
+    return np.broadcast_to(byte, (P, 512)), np.broadcast_to(shift, (P, 512))
 
 
 def rope_positions(bits_c, P):

@@ -41,7 +41,8 @@ def test_page_bytes_and_config_check(L):
     assert L.page_bytes(L.make_config(2, 64)) == 11520
     lib = L.lib()
     bad = [L.make_config(3, 128), L.make_config(4, 96), L.make_config(4, 128, n_recent=64),
-           L.make_config(4, 64, n_sink=17), L.make_config(4, 64, clip_q=1.5), L.make_config(4, 64, bits_r=2)]
+           L.make_config(4, 64, n_sink=17), L.make_config(4, 64, clip_q=1.5), L.make_config(4, 64, bits_r=2),
+           L.make_config(4, 16, n_recent=16)]
     for c in bad:
         assert lib.mla_qcache_config_check(ctypes.byref(c)) == -2
         assert L.page_bytes(c) == 0

@@ -61,8 +61,8 @@ def test_more_heads(heads):
 
 
 def test_no_sink_small_window_small_pages():
-    w = workloads.Workload("s0", 1, 16, 1, 4, 16, n_sink=0, n_recent=16, random_pages=True, seed=5)
-    _run(w, [500, 17, 16, 15])
+    w = workloads.Workload("s0", 1, 16, 1, 4, 32, n_sink=0, n_recent=32, random_pages=True, seed=5)
+    _run(w, [500, 33, 32, 31, 65, 64])
 
 
 def test_wide_window_and_sinks():

@@ -22,7 +22,7 @@ CASES = [  # bits_c, P, S, W, lengths
     (4, 128, 4, 128, [1024]),
     (4, 128, 4, 128, [1, 5, 127, 128, 129, 300]),
     (2, 64, 4, 128, [64, 63, 700, 131]),
-    (2, 16, 0, 16, [33, 17, 16]),
+    (2, 32, 0, 32, [65, 33, 32, 31]),
     (4, 32, 16, 64, [200, 3]),
     (2, 128, 4, 256, [1000]),
 ]
@@ -42,7 +42,7 @@ def test_bulk_prefill_bit_exact(bits_c, P, S, W, lens):
     assert cache.error_bits() == 0
 
 
-@pytest.mark.parametrize("bits_c,P,S,W", [(4, 16, 4, 32), (2, 64, 4, 128), (4, 128, 4, 128)])
+@pytest.mark.parametrize("bits_c,P,S,W", [(4, 32, 4, 32), (2, 64, 4, 128), (4, 128, 4, 128)])
 def test_decode_steps_fill_pages_and_evict(bits_c, P, S, W):
     """Prefill, then one token per sequence per call across page fills and window evictions
     (the single-launch writer path), checked after every call."""
@@ -102,7 +102,7 @@ def test_full_size_prefill_v2lite_shape():
 
 
 def test_device_error_bits():
-    w = _wl(4, 16, 4, 32)
+    w = _wl(4, 32, 4, 64)
     lens = np.array([40], np.int32)
     inp = workloads.make_inputs(w, seq_lens=lens)
     kw = w.config_kwargs()
@@ -115,7 +115,7 @@ def test_device_error_bits():
     assert cache.error_bits() & 1  # bad page
     # overflow of the page table
     cache2 = gu.gpu_cache(kw, inp)
-    cache2.seq_lens.fill_(inp.page_table.shape[1] * 16 - 2)
+    cache2.seq_lens.fill_(inp.page_table.shape[1] * 32 - 2)
     gu.write_rows(cache2, inp.c[:5], inp.kr[:5], np.array([5], np.int32), 5)
     torch.cuda.synchronize()
     assert cache2.error_bits() & 2

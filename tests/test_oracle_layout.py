@@ -105,27 +105,38 @@ def test_exhaustive_byte_roundtrip(bits_c):
         assert out == v
 
 
-def test_tensor_core_fragment_reading():
-    """The documented purpose of the latent layout: shifting a lane's word by 4*s and masking
-    the low nibble of each 16-bit half gives channels (2q,2q+1) [h=0] / (2q+8,2q+9) [h=1] of
-    chunk 2*word + s//2 of token t%8 (INT4)."""
-    P, bits_c = 16, 4
+@pytest.mark.parametrize("bits_c", [4, 2])
+def test_row_chunks_for_matrix_loads(bits_c):
+    """The documented purpose of the latent layout. Region A is token-major (one row of
+    64*bits_c bytes per token, channels in order inside the row), and the row's 16-byte chunks
+    are XOR-permuted by t mod 8. (1) For 8 consecutive tokens starting at a multiple of 8, the
+    same logical chunk lands on 8 distinct 16-byte positions modulo 128 bytes, so an 8x8
+    matrix load of 16-bit elements (one 16-byte row per token) touches every shared-memory
+    bank once. (2) The 16-bit little-endian element e of logical chunk j holds channels
+    32j + 4e + s at bits 4s (INT4) or 64j + 8e + i at bits 2i (INT2)."""
+    P = 32
     lb, ls = ld.latent_positions(bits_c, P)
+    row = 64 * bits_c
+    per_chunk = 128 // bits_c          # channels in a 16-byte chunk
+    per_elem = 16 // bits_c            # channels in a 16-bit element
+    for t0 in range(0, P, 8):
+        for j in range(row // 16):
+            c = j * per_chunk          # first channel of logical chunk j
+            starts = [(int(lb[t, c]) - t * row) for t in range(t0, t0 + 8)]
+            assert all(s0 % 16 == 0 for s0 in starts)
+            assert len({s0 % 128 for s0 in starts}) == 8
     rng = np.random.default_rng(0)
-    codes = rng.integers(0, 16, size=(P, 512))
+    codes = rng.integers(0, 1 << bits_c, size=(P, 512))
     page = np.zeros(ld.page_bytes(bits_c, P), dtype=np.uint8)
     for t in range(P):
         for c in range(512):
             page[lb[t, c]] |= codes[t, c] << ls[t, c]
-    for t in range(P):
-        g = 0
-        for lane_q in range(4):
-            lane = 4 * (t % 8) + lane_q
-            for word in range(4):
-                off = ((t // 8) * 4 + g) * 512 + lane * 16 + word * 4
-                w = int.from_bytes(page[off:off + 4].tobytes(), "little")
-                for s in range(4):
-                    lo, hi = (w >> (4 * s)) & 0xF, (w >> (16 + 4 * s)) & 0xF
-                    chunk = 2 * word + s // 2
-                    base = 16 * chunk + 2 * lane_q + 8 * (s % 2)
-                    assert (lo, hi) == (codes[t, base], codes[t, base + 1])
+    for t in range(0, P, 5):
+        for j in range(row // 16):
+            phys = j ^ (t % 8)
+            chunk = page[t * row + 16 * phys: t * row + 16 * phys + 16]
+            for e in range(8):
+                v = int(chunk[2 * e]) | (int(chunk[2 * e + 1]) << 8)
+                for s in range(per_elem):
+                    ch = j * per_chunk + per_elem * e + s
+                    assert (v >> (bits_c * s)) & ((1 << bits_c) - 1) == codes[t, ch]
