@@ -90,6 +90,12 @@ __device__ __forceinline__ float half_lo(uint32_t w) { return __half2float(__ush
 __device__ __forceinline__ float half_hi(uint32_t w) { return __half2float(__ushort_as_half(static_cast<uint16_t>(w >> 16))); }
 // 2^k as a float, k in [-126, 127]
 __device__ __forceinline__ float pow2i(int k) { return __uint_as_float(static_cast<uint32_t>(k + 127) << 23); }
+// 2^x, relative error below 2^-22 (hardware approximation; subnormal results flush to zero)
+__device__ __forceinline__ float exp2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 struct Shared {
   uint8_t* stages;  // packed stages, or BF16 row stages, or the output staging tile
@@ -442,7 +448,7 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
 
   // ---- query operands: FP16 with a per-head power-of-two prescale, in the masks' channel order
   uint32_t qa[8][4];
-  float qsum[2] = {0.f, 0.f}, f_lat[2];
+  float qsum[2] = {0.f, 0.f}, inv_f[2], head_scale;  // inv_f: prologue only
   {
     const uint16_t* r0 = p.q_lat + (static_cast<size_t>(b) * p.H + h0 + g) * kLatent + 128 * warp;
     const uint16_t* r1 = r0 + 8 * kLatent;
@@ -481,8 +487,20 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
     bool range = false;
     const int E0 = prescale_exponent(mx0, range), E1 = prescale_exponent(mx1, range);
     if (range) flags |= kErrRange;
-    f_lat[0] = pow2i(24 - E0);
-    f_lat[1] = pow2i(24 - E1);
+    // Partial scores are kept in units of 2^(24 - E) (the latent products' natural scale);
+    // the softmax lane of head 4w + lane/8 multiplies the sum back by that head's factor.
+    inv_f[0] = pow2i(E0 - 24);
+    inv_f[1] = pow2i(E1 - 24);
+    qsum[0] *= inv_f[0];
+    qsum[1] *= inv_f[1];
+    {
+      const int hh = 4 * warp + (lane >> 3);
+      float mh = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) mh = fmaxf(mh, sh.qmax[w * 16 + hh]);
+      bool r2 = false;
+      head_scale = p.scale_log2 * pow2i(24 - prescale_exponent(mh, r2));
+    }
 #pragma unroll
     for (int kc = 0; kc < 8; ++kc)
 #pragma unroll
@@ -508,6 +526,8 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
     qr[5] = bf16_hi(u1);
     qr[6] = bf16_lo(u3);
     qr[7] = bf16_hi(u3);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qr[e] *= inv_f[e >> 2];  // same units as the latent partials (exact)
   }
   // per-page rope factors: query times channel scale split into two BF16 terms
   uint32_t qr_hi[4], qr_lo[4];
@@ -528,7 +548,6 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
   }
   uint64_t* const xs_bar = sh.bars + kS;
   uint64_t* const xp_bar = sh.bars + kS + 2;
-  const float scale_log2 = p.scale_log2;
 
   // ---- scores of local tile i: partial sums over this warp's channels -> exchange buffer i&1
   auto score = [&](int i) {
@@ -587,14 +606,18 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
 #pragma unroll
       for (int nb = 0; nb < 4; ++nb) ldsm_x4(R[nb], sp + nb * 2048 + off_s);
 #pragma unroll
-      for (int m = 0; m < 4; ++m)
+      for (int m = 0; m < 4; ++m) {
+        uint32_t x8[4];
 #pragma unroll
         for (int nb = 0; nb < 4; ++nb) {
-          const uint32_t x = R[nb][m], x8 = x >> 8;
-          if (m == 0) mma_f16_16816_z(acc[nb], qa[0], x & 0x000f000fu, x8 & 0x000f000fu);
-          else mma_f16_16816(acc[nb], qa[2 * m], x & 0x000f000fu, x8 & 0x000f000fu);
-          mma_f16_16816(acc[nb], qa[2 * m + 1], x & 0x00f000f0u, x8 & 0x00f000f0u);
+          x8[nb] = R[nb][m] >> 8;
+          if (m == 0) mma_f16_16816_z(acc[nb], qa[0], R[nb][m] & 0x000f000fu, x8[nb] & 0x000f000fu);
+          else mma_f16_16816(acc[nb], qa[2 * m], R[nb][m] & 0x000f000fu, x8[nb] & 0x000f000fu);
         }
+#pragma unroll
+        for (int nb = 0; nb < 4; ++nb)
+          mma_f16_16816(acc[nb], qa[2 * m + 1], R[nb][m] & 0x00f000f0u, x8[nb] & 0x00f000f0u);
+      }
     } else {
       uint32_t R[4][2];
 #pragma unroll
@@ -625,37 +648,42 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
     }
     // k_R chunk `warp`: two 16-token blocks, BF16 integers 128 + code (exact)
     float racc[4][4];
+    uint32_t rb[4][2];
 #pragma unroll
     for (int tb = 0; tb < 2; ++tb) {
       const uint32_t w = *reinterpret_cast<const uint32_t*>(sp + G::kRopeOff + (tb * 4 + warp) * 128 + lane * 4);
 #pragma unroll
       for (int hb2 = 0; hb2 < 2; ++hb2) {
-        const uint32_t b0 = and_or(w >> (8 * hb2), 0x000f000fu, 0x43004300u);
-        const uint32_t b1 = and_or(w >> (8 * hb2 + 4), 0x000f000fu, 0x43004300u);
-        mma_bf16_16816_z(racc[2 * tb + hb2], qr_hi, b0, b1);
-        mma_bf16_16816(racc[2 * tb + hb2], qr_lo, b0, b1);
+        rb[2 * tb + hb2][0] = and_or(w >> (8 * hb2), 0x000f000fu, 0x43004300u);
+        rb[2 * tb + hb2][1] = and_or(w >> (8 * hb2 + 4), 0x000f000fu, 0x43004300u);
       }
     }
-    // token metadata of group `warp`: tokens 8nb + 2q + c
-    float* my = sh.sbuf + (buf * 4 + warp) * 16 * kXStride;
+    // token metadata of group `warp` (tokens 8nb + 2q + c): the min and bias terms seed the
+    // k_R accumulators, the scale multiplies the latent products
+    float tsc[4][2];
     bool big = false;
 #pragma unroll
-    for (int nb = 0; nb < 4; ++nb) {
-      float tsc[2], tmn[2];
+    for (int nb = 0; nb < 4; ++nb)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int tok = 8 * nb + 2 * q + c;
         const uint32_t w = *reinterpret_cast<const uint32_t*>(sp + G::kMetaOff + (tok * 4 + warp) * 4);
-        tsc[c] = half_lo(w);
-        tmn[c] = half_hi(w);
-        big |= tsc[c] >= kStrictScale;
+        const float tmn = half_hi(w);
+        tsc[nb][c] = half_lo(w);
+        big |= tsc[nb][c] >= kStrictScale;
+        racc[nb][c] = fmaf(tmn, qsum[0], rconst[0]);
+        racc[nb][2 + c] = fmaf(tmn, qsum[1], rconst[1]);
       }
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb) mma_bf16_16816(racc[nb], qr_hi, rb[nb][0], rb[nb][1]);
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb) mma_bf16_16816(racc[nb], qr_lo, rb[nb][0], rb[nb][1]);
+    float* my = sh.sbuf + (buf * 4 + warp) * 16 * kXStride;
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb) {
       float part[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = e >> 1, c = e & 1;
-        part[e] = fmaf(tsc[c] * f_lat[r], acc[nb][e], racc[nb][e] + fmaf(tmn[c], qsum[r], rconst[r]));
-      }
+      for (int e = 0; e < 4; ++e) part[e] = fmaf(tsc[nb][e & 1], acc[nb][e], racc[nb][e]);
       *reinterpret_cast<float2*>(my + g * kXStride + 8 * nb + 2 * q) = make_float2(part[0], part[1]);
       *reinterpret_cast<float2*>(my + (g + 8) * kXStride + 8 * nb + 2 * q) = make_float2(part[2], part[3]);
     }
@@ -681,10 +709,11 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
     }
     float lmax = -INFINITY;
     bool valid[4];
+    const bool inside = t0 >= lo && t0 + kPT <= hi;  // the common case: every token of the tile counts
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      valid[j] = (t0 + tt + j >= lo) && (t0 + tt + j < hi);
-      s[j] = valid[j] ? s[j] * scale_log2 : -INFINITY;
+      valid[j] = inside || ((t0 + tt + j >= lo) && (t0 + tt + j < hi));
+      s[j] = valid[j] ? s[j] * head_scale : -INFINITY;
       lmax = fmaxf(lmax, s[j]);
     }
     const float slack = strict ? 0.f : kRescaleSlack;
@@ -696,14 +725,14 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
 #pragma unroll
       for (int o = 1; o < 8; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
       if (tmax > st.m_run + slack || (st.m_run == -INFINITY && tmax > -INFINITY)) {
-        alpha = exp2f(st.m_run - tmax);  // 0 when the old reference was -inf
+        alpha = exp2_fast(st.m_run - tmax);  // 0 when the old reference was -inf
         st.l_part *= alpha;
         st.m_run = tmax;
       }
     }
     float pv[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) pv[j] = (valid[j] && st.m_run != -INFINITY) ? exp2f(s[j] - st.m_run) : 0.f;
+    for (int j = 0; j < 4; ++j) pv[j] = (valid[j] && st.m_run != -INFINITY) ? exp2_fast(s[j] - st.m_run) : 0.f;
     st.l_part += (pv[0] + pv[1]) + (pv[2] + pv[3]);
     *reinterpret_cast<float4*>(sh.pbuf + (buf * 16 + hh) * kXStride + tt) = make_float4(pv[0], pv[1], pv[2], pv[3]);
     if ((lane & 7) == 0) sh.alpha[buf * 16 + hh] = alpha;
@@ -772,22 +801,25 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
   };
 
   // ---- pipeline: scores of tile i+1 overlap the softmax exchange of tile i
-  if (n_my > 0) score(0);
-  for (int i = 0; i < n_my; ++i) {
+  // (i = -1 only computes the scores of tile 0, so the score code is inlined once)
+  for (int i = -1; i < n_my; ++i) {
     const int buf = i & 1;
     const uint32_t par = (i >> 1) & 1;
-    bool ok = mbar_wait_bounded(xs_bar + buf, par, kWaitBudget);
-    const int xf = sh.xflags[buf * 4] | sh.xflags[buf * 4 + 1] | sh.xflags[buf * 4 + 2] | sh.xflags[buf * 4 + 3];
-    if (!ok || (xf & 2)) {
-      flags |= kErrTimeout;
-      if (threadIdx.x == 0)  // orderly exit: bounded waits for the copies still in flight
-        for (int j = i + 1; j < issued; ++j)
-          (void)mbar_wait_bounded(sh.bars + (j % kS), (j / kS) & 1, kWaitBudget >> 4);
-      break;
+    if (i >= 0) {
+      const bool ok = mbar_wait_bounded(xs_bar + buf, par, kWaitBudget);
+      const int xf = sh.xflags[buf * 4] | sh.xflags[buf * 4 + 1] | sh.xflags[buf * 4 + 2] | sh.xflags[buf * 4 + 3];
+      if (!ok || (xf & 2)) {
+        flags |= kErrTimeout;
+        if (threadIdx.x == 0)  // orderly exit: bounded waits for the copies still in flight
+          for (int j = i + 1; j < issued; ++j)
+            (void)mbar_wait_bounded(sh.bars + (j % kS), (j / kS) & 1, kWaitBudget >> 4);
+        break;
+      }
+      softmax(i, (xf & 1) != 0);
     }
-    softmax(i, (xf & 1) != 0);
     if (i + 1 < n_my) score(i + 1);
-    ok = mbar_wait_bounded(xp_bar + buf, par, kWaitBudget);
+    if (i < 0) continue;
+    const bool ok = mbar_wait_bounded(xp_bar + buf, par, kWaitBudget);
     if (!ok) {
       flags |= kErrTimeout;
       if (threadIdx.x == 0)
