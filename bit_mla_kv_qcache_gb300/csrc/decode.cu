@@ -58,7 +58,7 @@ struct Geom {
   static constexpr int kMetaOff = kLat + 1024;      // 32 tokens x 4 groups x (scale, min)
   static constexpr int kRMetaOff = kMetaOff + 512;  // 64 channels x (scale, min)
   static constexpr int kStage = kRMetaOff + 256;
-  static constexpr int kStages = BITS == 4 ? 4 : 7;
+  static constexpr int kStages = 4;  // a power of two: stage index and phase are shifts
   static constexpr int kRegion =
       cmax(cmax(kStages * kStage, 2 * kTile * kBf16RowBytes), 16 * kOutStride * 4);
 };
@@ -70,12 +70,24 @@ constexpr int kNumBars = 12;                       // >= stages + 4 exchange bar
 template <int BITS>
 __host__ __device__ constexpr int smem_bytes() {
   return Geom<BITS>::kRegion + (kXsFloats + kXpFloats + 2 * 16 + 4 * 16) * 4 + kNumBars * 8 +
-         (2 * 4 + 2 * 4 + 2) * 4 + kMaxSplitPages * 4;
+         (2 * 4 + 2 * 4 + 4) * 4 + kMaxSplitPages * 4 + kThreads * 8 * 4;
 }
 // kCtasPerSm CTAs (each with 1 KB reserved by the hardware) fit in an SM's 228 KB
 static_assert(kCtasPerSm * (smem_bytes<4>() + 1024) <= 228 * 1024 &&
                   kCtasPerSm * (smem_bytes<2>() + 1024) <= 228 * 1024, "shared memory per SM");
 static_assert(Geom<4>::kStages + 4 <= kNumBars && Geom<2>::kStages + 4 <= kNumBars, "barriers");
+template <int BITS>
+constexpr int xflags_offset() {
+  return Geom<BITS>::kRegion + (kXsFloats + kXpFloats + 2 * 16 + 4 * 16) * 4 + kNumBars * 8;
+}
+static_assert(xflags_offset<4>() % 16 == 0 && xflags_offset<2>() % 16 == 0, "vector loads of the exchange flags");
+template <int BITS>
+constexpr int qr_offset() {
+  return xflags_offset<BITS>() + (2 * 4 + 2 * 4 + 4) * 4 + kMaxSplitPages * 4;
+}
+static_assert(qr_offset<4>() % 16 == 0 && qr_offset<2>() % 16 == 0, "vector access of the k_R query slice");
+static_assert(qr_offset<4>() + kThreads * 8 * 4 == smem_bytes<4>() && qr_offset<2>() + kThreads * 8 * 4 == smem_bytes<2>(),
+              "shared-memory carve");
 static_assert(2 * 4 * 16 * kRowStride <= kXsFloats && 2 * 16 * kRowStride <= kXpFloats, "BF16 exchange");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -86,8 +98,8 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   const __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
-__device__ __forceinline__ float half_lo(uint32_t w) { return __half2float(__ushort_as_half(static_cast<uint16_t>(w & 0xffffu))); }
-__device__ __forceinline__ float half_hi(uint32_t w) { return __half2float(__ushort_as_half(static_cast<uint16_t>(w >> 16))); }
+__device__ __forceinline__ float half_lo(uint32_t w) { return __low2float(*reinterpret_cast<const __half2*>(&w)); }
+__device__ __forceinline__ float half_hi(uint32_t w) { return __high2float(*reinterpret_cast<const __half2*>(&w)); }
 // 2^k as a float, k in [-126, 127]
 __device__ __forceinline__ float pow2i(int k) { return __uint_as_float(static_cast<uint32_t>(k + 127) << 23); }
 // 2^x, relative error below 2^-22 (hardware approximation; subnormal results flush to zero)
@@ -103,11 +115,12 @@ struct Shared {
   float* pbuf;      // packed: [2][16 heads][kXStride]; BF16 path: [2][16][kRowStride]
   float* alpha;     // [2][16]
   float* qmax;      // [4 warps][16 heads]: per-warp query maxima (prologue)
-  uint64_t* bars;   // packed: stages full [kStages], scores ready [2], weights ready [2]
-  int* xflags;      // [2][4] per warp and tile: bit 0 strict (a token scale >= kStrictScale), bit 1 timeout
+  uint64_t* bars;   // packed: stages full [kStages], scores ready [2], weights ready [2] (every thread arrives)
+  int* xflags;      // [2][4] per warp and tile (16-byte aligned): bit 0 strict (a token scale >= kStrictScale), bit 1 timeout
   int* moved;       // [2][4] per warp and tile: a reference max moved (rescale the outputs)
-  int* strict;      // [2] BF16 path: per exchange buffer
+  int* strict;      // [2] BF16 path: per exchange buffer (+2 padding)
   int* pids;        // [kMaxSplitPages] physical page ids of the split's pages (packed path)
+  float* qr;        // [kThreads][8] k_R query slice of each thread (read when the page changes)
 };
 
 template <int BITS>
@@ -122,7 +135,8 @@ __device__ __forceinline__ Shared carve(uint8_t* smem) {
   s.xflags = reinterpret_cast<int*>(s.bars + kNumBars);
   s.moved = s.xflags + 2 * 4;
   s.strict = s.moved + 2 * 4;
-  s.pids = s.strict + 2;
+  s.pids = s.strict + 4;  // strict padded to 16 bytes: pids and qr stay 16-byte aligned
+  s.qr = reinterpret_cast<float*>(s.pids + kMaxSplitPages);
   return s;
 }
 
@@ -512,9 +526,9 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
         qa[kc][2 * j + 1] = pack_f16x2(bf16_lo(v1) * s1, bf16_hi(v1) * s1);
       }
   }
-  // k_R query slice: rows g, g+8, dims 16w + {2q, 2q+1, 2q+8, 2q+9}
-  float qr[8];
+  // k_R query slice: rows g, g+8, dims 16w + {2q, 2q+1, 2q+8, 2q+9}, kept in shared memory
   {
+    float qr[8];
     const uint32_t* r0 = reinterpret_cast<const uint32_t*>(p.q_rope + (static_cast<size_t>(b) * p.H + h0 + g) * kRope + 16 * warp);
     const uint32_t* r1 = r0 + 8 * kRope / 2;
     const uint32_t u0 = __ldg(r0 + q), u1 = __ldg(r1 + q), u2 = __ldg(r0 + 4 + q), u3 = __ldg(r1 + 4 + q);
@@ -528,6 +542,9 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
     qr[7] = bf16_hi(u3);
 #pragma unroll
     for (int e = 0; e < 8; ++e) qr[e] *= inv_f[e >> 2];  // same units as the latent partials (exact)
+    float4* dst = reinterpret_cast<float4*>(sh.qr + threadIdx.x * 8);
+    dst[0] = make_float4(qr[0], qr[1], qr[2], qr[3]);
+    dst[1] = make_float4(qr[4], qr[5], qr[6], qr[7]);
   }
   // per-page rope factors: query times channel scale split into two BF16 terms
   uint32_t qr_hi[4], qr_lo[4];
@@ -566,6 +583,13 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
         const uint32_t w = rm[dims[e]];
         sc[e] = half_lo(w);
         mn[e] = half_hi(w);
+      }
+      float qr[8];
+      {
+        const float4 a = reinterpret_cast<const float4*>(sh.qr + threadIdx.x * 8)[0];
+        const float4 c = reinterpret_cast<const float4*>(sh.qr + threadIdx.x * 8)[1];
+        qr[0] = a.x; qr[1] = a.y; qr[2] = a.z; qr[3] = a.w;
+        qr[4] = c.x; qr[5] = c.y; qr[6] = c.z; qr[7] = c.w;
       }
       float hi_v[8], lo_v[8], rqs[2], rbias[2];
 #pragma unroll
@@ -689,8 +713,7 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
     }
     big = __any_sync(0xffffffffu, big);
     if (lane == 0) sh.xflags[buf * 4 + warp] = (big ? 1 : 0) | (ok ? 0 : 2);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(xs_bar + buf);
+    mbar_arrive(xs_bar + buf);
   };
 
   // ---- online softmax of tile i: heads 4w..4w+3, lane -> head 4w + lane/8, tokens 4*(lane%8)..+3
@@ -737,8 +760,7 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
     *reinterpret_cast<float4*>(sh.pbuf + (buf * 16 + hh) * kXStride + tt) = make_float4(pv[0], pv[1], pv[2], pv[3]);
     if ((lane & 7) == 0) sh.alpha[buf * 16 + hh] = alpha;
     if (lane == 0) sh.moved[buf * 4 + warp] = moved ? 1 : 0;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(xp_bar + buf);
+    mbar_arrive(xp_bar + buf);
     return moved;
   };
 
@@ -807,7 +829,8 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
     const uint32_t par = (i >> 1) & 1;
     if (i >= 0) {
       const bool ok = mbar_wait_bounded(xs_bar + buf, par, kWaitBudget);
-      const int xf = sh.xflags[buf * 4] | sh.xflags[buf * 4 + 1] | sh.xflags[buf * 4 + 2] | sh.xflags[buf * 4 + 3];
+      const int4 xv = *reinterpret_cast<const int4*>(sh.xflags + buf * 4);
+      const int xf = (xv.x | xv.y) | (xv.z | xv.w);
       if (!ok || (xf & 2)) {
         flags |= kErrTimeout;
         if (threadIdx.x == 0)  // orderly exit: bounded waits for the copies still in flight
@@ -835,7 +858,8 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
       }
       ++issued;
     }
-    if (sh.moved[buf * 4] | sh.moved[buf * 4 + 1] | sh.moved[buf * 4 + 2] | sh.moved[buf * 4 + 3]) {
+    const int4 mv = *reinterpret_cast<const int4*>(sh.moved + buf * 4);
+    if ((mv.x | mv.y) | (mv.z | mv.w)) {
       const float a0 = sh.alpha[buf * 16 + g], a1 = sh.alpha[buf * 16 + g + 8];
 #pragma unroll
       for (int cb = 0; cb < 16; ++cb) {
@@ -937,9 +961,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
     if (is_bf16) {  // two row stages, one arrival each
       mbar_init(sh.bars, 1);
       mbar_init(sh.bars + 1, 1);
-    } else {  // packed stages (one arrival + bytes), then the exchanges (one arrival per warp)
+    } else {  // packed stages (one arrival + bytes), then the exchanges (one arrival per thread)
       for (int i = 0; i < Geom<BITS>::kStages; ++i) mbar_init(sh.bars + i, 1);
-      for (int i = 0; i < 4; ++i) mbar_init(sh.bars + Geom<BITS>::kStages + i, 4);
+      for (int i = 0; i < 4; ++i) mbar_init(sh.bars + Geom<BITS>::kStages + i, kThreads);
     }
     fence_mbar_init();
     sh.strict[0] = sh.strict[1] = 0;
