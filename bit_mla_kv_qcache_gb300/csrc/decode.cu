@@ -424,6 +424,7 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
     const int tile_end = first + static_cast<int>((static_cast<long long>(n_total) * (split + 1)) / p.n_split);
     n_my = tile_end - tile_begin;
   }
+  if (n_my == 0) return;  // empty share (a short sequence): the merge sees sum 0 and skips it
   const int pg0 = (tile_begin * kPT) >> p.p_shift;
   // validate the page ids this split reads; a bad id drops the split's work
   {
@@ -946,10 +947,12 @@ template <int BITS>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const Shared sh = carve<BITS>(smem);
-  const int split = blockIdx.x, b = blockIdx.z;
+  // grid (B, H/16, n_split + 1): z = 0 serves the protected tokens, z >= 1 packed share z - 1, so
+  // the hardware dispatches the protected CTAs first and then the shares split by split
+  const bool is_bf16 = blockIdx.z == 0;
+  const int split = is_bf16 ? p.n_split : static_cast<int>(blockIdx.z) - 1, b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h0 = blockIdx.y * 16;
-  const bool is_bf16 = split == p.n_split;
   int32_t flags = 0;
 
   int T = __ldg(p.seq_lens + b);
@@ -1041,6 +1044,12 @@ int decode_num_splits(int B, int H, int max_pages, int P, int num_sms) {
   const int target = kCtasPerSm * num_sms;  // one full wave of resident CTAs
   int ns = target / (groups > 0 ? groups : 1) - 1;
   const long long max_sub = (static_cast<long long>(max_pages) * P) / kPT;
+  // Long page tables get splits of at most ~kShareTiles tiles even past one wave: a ragged batch
+  // then spreads its longest sequences over many CTAs while the shares of short sequences are
+  // empty and exit at once, and the hardware backfills the SMs (split-major dispatch).
+  constexpr int kShareTiles = 80;
+  const long long by_len = (max_sub + kShareTiles - 1) / kShareTiles;
+  if (by_len > ns) ns = static_cast<int>(by_len > 64 ? 64 : by_len);
   int cap = static_cast<int>(max_sub / 4);
   if (cap < 1) cap = 1;
   if (ns > cap) ns = cap;
@@ -1072,7 +1081,7 @@ cudaError_t ensure_smem_attr() {
 }
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
-  const dim3 grid(p.n_split + 1, p.H / 16, p.B);
+  const dim3 grid(p.B, p.H / 16, p.n_split + 1);
   cudaError_t e;
   if (p.bits_c == 4) {
     if ((e = ensure_smem_attr<4>()) != cudaSuccess) return e;

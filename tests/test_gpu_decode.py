@@ -77,6 +77,18 @@ def test_ragged_batch_c2r4_serving_shape():
     _run(w, lens)
 
 
+def test_many_sequences_work_split():
+    """More sequences than a CTA has threads (the device-side scan of packed tile counts runs
+    over several chunks), with sequences that have no packed tokens, short and long ones: the
+    packed CTAs are shared in proportion to each sequence's tiles."""
+    rng = np.random.default_rng(5)
+    lens = rng.integers(0, 900, size=300)
+    lens[::7] = 0
+    lens[::11] = 132
+    lens[::13] = 133
+    _run(C4, lens)
+
+
 def test_peaked_softmax():
     """A large softmax scale concentrates the weights (stresses the running-max rescaling)."""
     _run(C4, [600, 250], scale=0.5)
