@@ -51,7 +51,8 @@ size_t mla_qcache_workspace_bytes(const mla_qcache_config* cfg, int32_t B, int32
   int sms = 0;
   if (current_sm_count(&sms) != MLA_QCACHE_OK) return 0;
   const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, sms);
-  return mlaq::decode_workspace_bytes(B, H, ns);
+  const int nq = mlaq::decode_num_protected(B, H, max_pages, cfg->page_size, cfg->n_sink, cfg->n_recent, sms);
+  return mlaq::decode_workspace_bytes(B, H, ns + nq);
 }
 
 int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, const uint16_t* c_new,
@@ -140,7 +141,8 @@ int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H, c
   st = current_sm_count(&sms);
   if (st != MLA_QCACHE_OK) return st;
   const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, sms);
-  const size_t need = mlaq::decode_workspace_bytes(B, H, ns);
+  const int nq = mlaq::decode_num_protected(B, H, max_pages, cfg->page_size, cfg->n_sink, cfg->n_recent, sms);
+  const size_t need = mlaq::decode_workspace_bytes(B, H, ns + nq);
   if (workspace_bytes < need) return MLA_QCACHE_ERR_WORKSPACE;
 
   mlaq::DecodeParams p{};
@@ -152,7 +154,7 @@ int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H, c
   p.sink = sink_buf;
   p.ring = recent_buf;
   p.o_part = static_cast<float*>(workspace);
-  p.ml_part = static_cast<float*>(workspace) + static_cast<size_t>(B) * H * (ns + 1) * mlaq::kLatent;
+  p.ml_part = static_cast<float*>(workspace) + static_cast<size_t>(B) * H * (ns + nq) * mlaq::kLatent;
   p.out = out;
   p.lse = lse;
   p.err = err_word;
@@ -169,6 +171,7 @@ int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H, c
   p.W = cfg->n_recent;
   p.bits_c = cfg->bits_c;
   p.n_split = ns;
+  p.n_q = nq;
   const cudaError_t e = mlaq::launch_decode(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
 }
@@ -186,7 +189,8 @@ int mla_qcache_decode_attn_noalloc(const mla_qcache_config* cfg, int32_t B, int3
   st = current_sm_count(&sms);
   if (st != MLA_QCACHE_OK) return st;
   const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, sms);
-  if (mlaq::decode_workspace_bytes(B, H, ns) > mlaq::kNoAllocScratchBytes) return MLA_QCACHE_ERR_SCRATCH_LIMIT;
+  const int nq = mlaq::decode_num_protected(B, H, max_pages, cfg->page_size, cfg->n_sink, cfg->n_recent, sms);
+  if (mlaq::decode_workspace_bytes(B, H, ns + nq) > mlaq::kNoAllocScratchBytes) return MLA_QCACHE_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   if (mlaq::noalloc_scratch(&scratch) != cudaSuccess) return MLA_QCACHE_ERR_CUDA;
   return mla_qcache_decode_attn(cfg, B, H, q_lat, q_rope, page_table, max_pages, seq_lens, pool, n_pages, sink_buf,

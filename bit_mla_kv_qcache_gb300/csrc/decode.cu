@@ -1,10 +1,11 @@
 // Decode attention over the low-bit dual-path MLA cache (QuantMLA page, abstract and appendix
 // Figure 8; RAQ-MLA page, Figures 3-4 and appendix Table 5).
 //
-// Grid (n_split + 1, H/16, B). CTA (s, hb, b) handles 16 heads of sequence b:
-//   s <  n_split : an even share of the packed tokens [S, T-W), in tiles of 32 tokens streamed
-//                  from the page pool into a ring of shared-memory stages by bulk copies;
-//   s == n_split : the protected tokens (t < S or t >= T-W) from the BF16 sink/recent buffers.
+// Grid (B, H/16, n_q + n_split). CTA (b, hb, z) handles 16 heads of sequence b:
+//   z <  n_q : a share of the protected tokens (t < S or t >= T-W) from the BF16 sink/recent
+//              buffers (n_q > 1 only when there is little packed work);
+//   z >= n_q : share z - n_q of the packed tokens [S, T-W), in tiles of 32 tokens streamed from
+//              the page pool into a ring of shared-memory stages by bulk copies.
 // Each CTA writes an unnormalized partial (O, max, sum); a second kernel merges the partials
 // with a log-sum-exp reduction (one global softmax over all tokens).
 //
@@ -238,17 +239,21 @@ __device__ __forceinline__ void load_p(const Shared& sh, int buf, float2 (&pf)[4
 }
 
 // ------------------------------------------------------------------ protected (BF16) tokens
-__device__ void bf16_split(const DecodeParams& p, const Shared& sh, int b, int T, const uint32_t (&qa)[8][4],
-                           const uint32_t (&qra)[4], State& st, int32_t& flags) {
+__device__ void bf16_split(const DecodeParams& p, const Shared& sh, int b, int T, int part,
+                           const uint32_t (&qa)[8][4], const uint32_t (&qra)[4], State& st, int32_t& flags) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s_end = min(p.S, T);
   const int r_beg = max(T - p.W, s_end);
   const int has_sink = s_end > 0 ? 1 : 0;
-  const int n_tiles = has_sink + (T - r_beg + kTile - 1) / kTile;
+  const int n_all = has_sink + (T - r_beg + kTile - 1) / kTile;
+  // this CTA's share of the sequence's protected tiles: [t_lo, t_lo + n_tiles)
+  const int t_lo = (n_all * part) / p.n_q;
+  const int n_tiles = (n_all * (part + 1)) / p.n_q - t_lo;
   if (n_tiles <= 0) return;
   constexpr int kStageBytes = kTile * kBf16RowBytes;
 
-  auto tile_range = [&](int i, int& start, int& count) {
+  auto tile_range = [&](int li, int& start, int& count) {  // li: index in this CTA's share
+    const int i = t_lo + li;
     if (has_sink && i == 0) {
       start = 0;
       count = s_end;
@@ -896,7 +901,7 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
     }
   }
   __syncthreads();
-  const int NS = p.n_split + 1;
+  const int NS = p.n_split + p.n_q;
   for (int idx = threadIdx.x; idx < 16 * (kLatent / 4); idx += kThreads) {
     const int row = idx / (kLatent / 4), c4 = idx % (kLatent / 4);
     const float4 v = *reinterpret_cast<const float4*>(tile + row * kOutStride + 4 * c4);
@@ -905,7 +910,8 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
 }
 
 // ------------------------------------------------------------------ protected-token CTA
-__device__ void protected_split(const DecodeParams& p, const Shared& sh, int b, int T, State& st, int32_t& flags) {
+__device__ void protected_split(const DecodeParams& p, const Shared& sh, int b, int T, int part, State& st,
+                                int32_t& flags) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
   const int h0 = blockIdx.y * 16;
   // query fragments for latent group `warp` (BF16, exact, channels in order)
@@ -931,11 +937,11 @@ __device__ void protected_split(const DecodeParams& p, const Shared& sh, int b, 
     qra[2] = __ldg(r0 + 4 + q);
     qra[3] = __ldg(r1 + 4 + q);
   }
-  bf16_split(p, sh, b, T, qa, qra, st, flags);
+  bf16_split(p, sh, b, T, part, qa, qra, st, flags);
 
-  const int NS = p.n_split + 1;
-  float* o0 = p.o_part + ((static_cast<size_t>(b) * p.H + h0 + g) * NS + p.n_split) * kLatent + 128 * warp;
-  float* o1 = p.o_part + ((static_cast<size_t>(b) * p.H + h0 + g + 8) * NS + p.n_split) * kLatent + 128 * warp;
+  const int NS = p.n_split + p.n_q, slot = p.n_split + part;
+  float* o0 = p.o_part + ((static_cast<size_t>(b) * p.H + h0 + g) * NS + slot) * kLatent + 128 * warp;
+  float* o1 = p.o_part + ((static_cast<size_t>(b) * p.H + h0 + g + 8) * NS + slot) * kLatent + 128 * warp;
 #pragma unroll
   for (int cb = 0; cb < 16; ++cb) {
     *reinterpret_cast<float2*>(o0 + 8 * cb + 2 * q) = make_float2(st.o[cb][0], st.o[cb][1]);
@@ -947,10 +953,12 @@ template <int BITS>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const Shared sh = carve<BITS>(smem);
-  // grid (B, H/16, n_split + 1): z = 0 serves the protected tokens, z >= 1 packed share z - 1, so
-  // the hardware dispatches the protected CTAs first and then the shares split by split
-  const bool is_bf16 = blockIdx.z == 0;
-  const int split = is_bf16 ? p.n_split : static_cast<int>(blockIdx.z) - 1, b = blockIdx.x;
+  // grid (B, H/16, n_q + n_split): z < n_q serves a share of the protected tokens, z >= n_q packed
+  // share z - n_q, so the hardware dispatches the protected CTAs first and then the shares split
+  // by split. Partial slot: packed share s -> s, protected share q -> n_split + q.
+  const bool is_bf16 = static_cast<int>(blockIdx.z) < p.n_q;
+  const int split = is_bf16 ? p.n_split + static_cast<int>(blockIdx.z) : static_cast<int>(blockIdx.z) - p.n_q;
+  const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h0 = blockIdx.y * 16;
   int32_t flags = 0;
@@ -980,10 +988,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
   st.m_run = -INFINITY;
   st.l_part = 0.f;
 
-  if (is_bf16) protected_split(p, sh, b, T, st, flags);
+  if (is_bf16) protected_split(p, sh, b, T, split - p.n_split, st, flags);
   else packed_split<BITS>(p, sh, b, T, split, st, flags);
 
-  const int NS = p.n_split + 1;
+  const int NS = p.n_split + p.n_q;
   float l_run = st.l_part;
 #pragma unroll
   for (int o = 1; o < 8; o <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, o);
@@ -1001,7 +1009,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
 // the split maxima and sums, then a weighted sum of the partial outputs.
 __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p) {
   const int bh = blockIdx.x;
-  const int NS = p.n_split + 1;
+  const int NS = p.n_split + p.n_q;
   const int lane = threadIdx.x & 31;
   const float* ml = p.ml_part + static_cast<size_t>(bh) * NS * 2;
   float m = -INFINITY;
@@ -1058,8 +1066,21 @@ int decode_num_splits(int B, int H, int max_pages, int P, int num_sms) {
   return ns;
 }
 
-size_t decode_workspace_bytes(int B, int H, int n_split) {
-  const size_t NS = static_cast<size_t>(n_split) + 1;
+int decode_num_protected(int B, int H, int max_pages, int P, int S, int W, int num_sms) {
+  // Little packed work per CTA: the protected tiles would be the critical path of one CTA,
+  // so they are shared by several (one 16-row tile each at most).
+  const long long groups = static_cast<long long>(B) * (H / 16);
+  const long long wave = static_cast<long long>(kCtasPerSm) * (num_sms > 0 ? num_sms : 1);
+  const long long prot_max = (S > 0 ? 1 : 0) + (W + kTile - 1) / kTile;
+  const long long T = static_cast<long long>(max_pages) * P;
+  const long long packed_max = T > S + W ? (T - W - 1) / kPT - S / kPT + 1 : 0;
+  if (2 * groups * packed_max >= wave * prot_max) return 1;
+  long long nq = wave / (4 * groups);
+  return static_cast<int>(nq < 1 ? 1 : (nq > prot_max ? prot_max : nq));
+}
+
+size_t decode_workspace_bytes(int B, int H, int n_slots) {
+  const size_t NS = static_cast<size_t>(n_slots);
   return static_cast<size_t>(B) * H * NS * (kLatent + 2) * sizeof(float);
 }
 
@@ -1081,7 +1102,7 @@ cudaError_t ensure_smem_attr() {
 }
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
-  const dim3 grid(p.B, p.H / 16, p.n_split + 1);
+  const dim3 grid(p.B, p.H / 16, p.n_q + p.n_split);
   cudaError_t e;
   if (p.bits_c == 4) {
     if ((e = ensure_smem_attr<4>()) != cudaSuccess) return e;

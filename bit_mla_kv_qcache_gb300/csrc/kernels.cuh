@@ -59,12 +59,15 @@ struct DecodeParams {
   float scale_log2;  // softmax_scale * log2(e)
   int B, H, max_pages, P, S, W, bits_c;
   int p_shift;  // log2(P): page sizes are powers of two
-  int n_split;  // splits of the packed tokens; split index n_split is the BF16 (protected) split
+  int n_split;  // shares of the packed tokens (partial slots 0 .. n_split-1)
+  int n_q;      // CTAs sharing the protected (BF16) tokens (partial slots n_split .. n_split+n_q-1)
 };
 
-// Number of packed-token splits for a problem size (depends on the SM count).
+// Number of packed-token shares, and of CTAs for the protected tokens, of each (sequence,
+// 16-head block) for a problem size (depends on the SM count).
 int decode_num_splits(int B, int H, int max_pages, int P, int num_sms);
-size_t decode_workspace_bytes(int B, int H, int n_split);
+int decode_num_protected(int B, int H, int max_pages, int P, int S, int W, int num_sms);
+size_t decode_workspace_bytes(int B, int H, int n_slots);  // n_slots = n_split + n_q
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 
 // Built-in decode scratch for callers that cannot allocate (mla_qcache_decode_attn_noalloc).
