@@ -1025,14 +1025,25 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (m != -INFINITY && l > 0.f) {
     const float* op = p.o_part + static_cast<size_t>(bh) * NS * kLatent + 4 * threadIdx.x;
-    for (int s = 0; s < NS; ++s) {
-      const float w = exp2f(ml[2 * s] - m);
-      if (w == 0.f) continue;
-      const float4 v = *reinterpret_cast<const float4*>(op + static_cast<size_t>(s) * kLatent);
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
+    // eight independent loads in flight per batch (the partials are read once, mostly from L2)
+    constexpr int kBatch = 8;
+    for (int s0 = 0; s0 < NS; s0 += kBatch) {
+      float w[kBatch];
+      float4 v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int sl = s0 + u;
+        w[u] = sl < NS ? exp2f(ml[2 * sl] - m) : 0.f;
+        v[u] = w[u] != 0.f ? *reinterpret_cast<const float4*>(op + static_cast<size_t>(sl) * kLatent)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        acc.x += w[u] * v[u].x;
+        acc.y += w[u] * v[u].y;
+        acc.z += w[u] * v[u].z;
+        acc.w += w[u] * v[u].w;
+      }
     }
     const float inv = 1.f / l;
     acc.x *= inv;
