@@ -294,13 +294,12 @@ def run_native(args, w):
     out = torch.empty((B, H, 512), dtype=torch.float32, device=dev)
     lse = torch.empty((B, H), dtype=torch.float32, device=dev)
     ws_buf = caches[0].workspace(H)
-    one = torch.ones(B, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
     def write_step(cache):
         q.mla_qcache_write(cfg, c_new, kr_new, cu1, cache.seq_lens, 1, cache.page_table, cache.pool, cache.sink,
                            cache.ring, cache.err)
-        cache.seq_lens.add_(one)
+        q.mla_qcache_advance(cu1, cache.seq_lens)
 
     def decode_step(cache):
         q.mla_qcache_decode_attn(cfg, q_lat, q_rope, cache.page_table, cache.seq_lens, cache.pool, cache.sink,
@@ -377,7 +376,7 @@ def run_native(args, w):
                      "frac": achieved / hbm_peak, "traffic": traffic,
                      "kernel": "mla_qcache_decode_attn (decode_kernel + combine_kernel)",
                      "algorithmic_bytes_per_call": bytes_dec, "peak_kind": peak_kind},
-        "gpu_launches": 3 * args.steps,  # per step: write_kernel, decode_kernel, combine_kernel
+        "gpu_launches": 4 * args.steps,  # per step: write_kernel, advance_kernel, decode_kernel, combine_kernel
         "clocks": clk.summary(),
     }
 

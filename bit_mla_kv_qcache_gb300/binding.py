@@ -20,7 +20,7 @@ DEV_BAD_PAGE, DEV_SEQ_OVERFLOW, DEV_NONFINITE, DEV_RANGE, DEV_ROWS, DEV_TIMEOUT 
 # the entry points declared in include/mla_qcache.h
 EXPORTS = ("mla_qcache_page_bytes", "mla_qcache_config_check", "mla_qcache_workspace_bytes",
            "mla_qcache_write", "mla_qcache_decode_attn", "mla_qcache_strerror",
-           "mla_qcache_decode_attn_noalloc", "mla_qcache_noalloc_scratch_bytes")
+           "mla_qcache_decode_attn_noalloc", "mla_qcache_noalloc_scratch_bytes", "mla_qcache_advance")
 
 
 class Config(ctypes.Structure):
@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
                                                      ctypes.c_float, vp, vp, vp, vp]
         L.mla_qcache_noalloc_scratch_bytes.restype = sz
         L.mla_qcache_noalloc_scratch_bytes.argtypes = []
+        L.mla_qcache_advance.restype = ctypes.c_int
+        L.mla_qcache_advance.argtypes = [vp, vp, i32, vp]
         L.mla_qcache_strerror.restype = ctypes.c_char_p
         L.mla_qcache_strerror.argtypes = [i32]
         _lib = L
@@ -128,6 +130,13 @@ def mla_qcache_write(cfg: Config, c_new, kr_new, cu_new, seq_lens, max_new: int,
         pool.shape[0], _ptr(sink_buf, "sink_buf", 2, allow_none=True) if cfg.n_sink else None,
         _ptr(recent_buf, "recent_buf", 2), _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
     _raise(st, "mla_qcache_write")
+
+
+def mla_qcache_advance(cu_new, seq_lens, stream=None) -> None:
+    """seq_lens[b] += cu_new[b+1] - cu_new[b] on the device (see include/mla_qcache.h)."""
+    st = lib().mla_qcache_advance(_ptr(cu_new, "cu_new", dtype=torch.int32),
+                                  _ptr(seq_lens, "seq_lens", dtype=torch.int32), seq_lens.shape[0], _stream(stream))
+    _raise(st, "mla_qcache_advance")
 
 
 def mla_qcache_decode_attn(cfg: Config, q_lat, q_rope, page_table, seq_lens, pool, sink_buf, recent_buf,

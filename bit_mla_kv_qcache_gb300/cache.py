@@ -36,6 +36,7 @@ class QuantizedMLACache:
         self.seq_lens = torch.zeros(batch, dtype=torch.int32, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self._ws = None
+        self._ws_need = {}  # workspace bytes per head count
 
     def write(self, c_new: torch.Tensor, kr_new: torch.Tensor, cu_new: torch.Tensor, max_new: int,
               advance: bool = True, stream=None) -> None:
@@ -43,10 +44,12 @@ class QuantizedMLACache:
         binding.mla_qcache_write(self.cfg, c_new, kr_new, cu_new, self.seq_lens, max_new, self.page_table, self.pool,
                                  self.sink, self.ring, self.err, stream)
         if advance:
-            self.seq_lens += (cu_new[1:] - cu_new[:-1]).to(torch.int32)
+            binding.mla_qcache_advance(cu_new, self.seq_lens, stream)
 
     def workspace(self, heads: int) -> torch.Tensor:
-        need = binding.workspace_bytes(self.cfg, self.B, heads, self.max_pages)
+        need = self._ws_need.get(heads)
+        if need is None:
+            need = self._ws_need[heads] = binding.workspace_bytes(self.cfg, self.B, heads, self.max_pages)
         if self._ws is None or self._ws.numel() < need:
             self._ws = torch.empty(max(need, 16), dtype=torch.uint8, device=self.pool.device)
         return self._ws

@@ -120,6 +120,14 @@ int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, co
   return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
 }
 
+int mla_qcache_advance(const int32_t* cu_new, int32_t* seq_lens, int32_t B, void* stream) {
+  if (!cu_new || !seq_lens) return MLA_QCACHE_ERR_NULL;
+  if (B < 1) return MLA_QCACHE_ERR_SHAPE;
+  if (!aligned(cu_new, 4) || !aligned(seq_lens, 4)) return MLA_QCACHE_ERR_ALIGN;
+  const cudaError_t e = mlaq::launch_advance(cu_new, seq_lens, B, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
+}
+
 int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H, const uint16_t* q_lat,
                            const uint16_t* q_rope, const int32_t* page_table, int32_t max_pages,
                            const int32_t* seq_lens, const uint8_t* pool, int64_t n_pages,

@@ -40,6 +40,8 @@ struct WriteParams {
 
 // One launch doing per-token packing/retention (token_blocks > 0) and/or page fills.
 cudaError_t launch_write(const WriteParams& p, cudaStream_t stream);
+// seq_lens[b] += cu_new[b+1] - cu_new[b] for b in [0, B).
+cudaError_t launch_advance(const int32_t* cu_new, int32_t* seq_lens, int B, cudaStream_t stream);
 
 struct DecodeParams {
   const uint16_t* q_lat;

@@ -319,7 +319,17 @@ __global__ void __launch_bounds__(128) write_kernel(const WriteParams p) {
   if (b < p.B) fill_page(p, b, f, smem_f, smem_f + p.P * 65);
 }
 
+__global__ void __launch_bounds__(256) advance_kernel(const int32_t* cu_new, int32_t* seq_lens, int B) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) seq_lens[b] += __ldg(cu_new + b + 1) - __ldg(cu_new + b);
+}
+
 }  // namespace
+
+cudaError_t launch_advance(const int32_t* cu_new, int32_t* seq_lens, int B, cudaStream_t stream) {
+  advance_kernel<<<(B + 255) / 256, 256, 0, stream>>>(cu_new, seq_lens, B);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_write(const WriteParams& p, cudaStream_t stream) {
   const int blocks = p.token_blocks + p.B * p.fill_per_seq;

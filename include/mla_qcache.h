@@ -187,6 +187,16 @@ int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows,
                      uint16_t* recent_buf, int32_t* err_word, void* stream);
 
 /*
+ * Length update after a write (the pages leave the bookkeeping to the caller): for every
+ * sequence b in [0, B), seq_lens[b] += cu_new[b+1] - cu_new[b], in one kernel on `stream`,
+ * ordered after a preceding mla_qcache_write on the same stream. cu_new [B+1] and seq_lens [B]
+ * are device int32 arrays, 4-byte aligned; seq_lens must not be read by a write still in flight
+ * on another stream.
+ * Errors: NULL pointer or B < 1 -> negative status, nothing run.
+ */
+int mla_qcache_advance(const int32_t* cu_new, int32_t* seq_lens, int32_t B, void* stream);
+
+/*
  * Decode attention over the quantized dual-path cache ([QuantMLA] abstract and Figure 8;
  * [RAQ-MLA] Figures 3-4: absorbed query, score = q_lat . c + q_rope . k_R, latent-space
  * readout).

@@ -80,6 +80,11 @@ def test_host_validation_without_gpu(L):
     bad = L.make_config(4, 128, n_recent=64)
     assert lib.mla_qcache_decode_attn(ctypes.byref(bad), 1, 16, p, p, p, 1, p, p, 1, p, p, f, p, p, p, 1 << 20, p,
                                       None) == -2
+    # length update: NULL pointers, B < 1, misaligned arrays are rejected before any launch
+    assert lib.mla_qcache_advance(None, p, 4, None) == -1
+    assert lib.mla_qcache_advance(p, None, 4, None) == -1
+    assert lib.mla_qcache_advance(p, p, 0, None) == -3
+    assert lib.mla_qcache_advance(ctypes.c_void_p(16 * 1024 + 2), p, 4, None) == -4
 
 
 def test_product_path_has_no_cpu_fallback(L, monkeypatch):

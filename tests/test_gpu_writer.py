@@ -119,3 +119,13 @@ def test_device_error_bits():
     gu.write_rows(cache2, inp.c[:5], inp.kr[:5], np.array([5], np.int32), 5)
     torch.cuda.synchronize()
     assert cache2.error_bits() & 2
+
+
+def test_advance_lengths():
+    """mla_qcache_advance adds each sequence's new-row count to its length (one kernel)."""
+    import bit_mla_kv_qcache_gb300 as q
+    lens = torch.tensor([0, 5, 130, 7, 1 << 20], dtype=torch.int32, device="cuda")
+    cu = torch.tensor([0, 1, 1, 4, 10, 11], dtype=torch.int32, device="cuda")
+    q.mla_qcache_advance(cu, lens)
+    torch.cuda.synchronize()
+    assert lens.cpu().tolist() == [1, 5, 133, 13, (1 << 20) + 1]
