@@ -1012,6 +1012,15 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p) {
   const int NS = p.n_split + p.n_q;
   const int lane = threadIdx.x & 31;
   const float* ml = p.ml_part + static_cast<size_t>(bh) * NS * 2;
+  const float* op = p.o_part + static_cast<size_t>(bh) * NS * kLatent + 4 * threadIdx.x;
+  // The first batch of partial rows is requested together with the maxima (one round trip
+  // instead of two); a slot whose weight is zero is dropped by selection, never multiplied, as
+  // the row of an empty share holds whatever the buffer held before.
+  constexpr int kBatch = 8;
+  float4 v[kBatch];
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u)
+    v[u] = u < NS ? *reinterpret_cast<const float4*>(op + static_cast<size_t>(u) * kLatent) : make_float4(0.f, 0.f, 0.f, 0.f);
   float m = -INFINITY;
   for (int s = lane; s < NS; s += 32) m = fmaxf(m, ml[2 * s]);
 #pragma unroll
@@ -1024,25 +1033,22 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p) {
 
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (m != -INFINITY && l > 0.f) {
-    const float* op = p.o_part + static_cast<size_t>(bh) * NS * kLatent + 4 * threadIdx.x;
-    // eight independent loads in flight per batch (the partials are read once, mostly from L2)
-    constexpr int kBatch = 8;
     for (int s0 = 0; s0 < NS; s0 += kBatch) {
-      float w[kBatch];
-      float4 v[kBatch];
+      if (s0 > 0) {
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int sl = s0 + u;
-        w[u] = sl < NS ? exp2f(ml[2 * sl] - m) : 0.f;
-        v[u] = w[u] != 0.f ? *reinterpret_cast<const float4*>(op + static_cast<size_t>(sl) * kLatent)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < kBatch; ++u)
+          v[u] = s0 + u < NS ? *reinterpret_cast<const float4*>(op + static_cast<size_t>(s0 + u) * kLatent)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
-        acc.x += w[u] * v[u].x;
-        acc.y += w[u] * v[u].y;
-        acc.z += w[u] * v[u].z;
-        acc.w += w[u] * v[u].w;
+        const float w = s0 + u < NS ? exp2f(ml[2 * (s0 + u)] - m) : 0.f;
+        if (w != 0.f) {
+          acc.x += w * v[u].x;
+          acc.y += w * v[u].y;
+          acc.z += w * v[u].z;
+          acc.w += w * v[u].w;
+        }
       }
     }
     const float inv = 1.f / l;
