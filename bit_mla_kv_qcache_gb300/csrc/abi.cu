@@ -64,6 +64,9 @@ int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, co
   if (B < 1 || B > (1 << 20) || n_rows < 0 || max_pages < 1 || n_pages < 1) return MLA_QCACHE_ERR_SHAPE;
   if (n_rows == 0) return MLA_QCACHE_OK;
   if (max_new < 1) return MLA_QCACHE_ERR_SHAPE;
+  // one CTA per row plus four per page that may fill, in one grid dimension
+  if (static_cast<int64_t>(B) * (max_new / cfg->page_size + 1) * 4 + n_rows > 0x7fffffff)
+    return MLA_QCACHE_ERR_SHAPE;
   if (!c_new || !kr_new || !cu_new || !seq_lens || !page_table || !pool || !recent_buf || !err_word)
     return MLA_QCACHE_ERR_NULL;
   if (cfg->n_sink > 0 && !sink_buf) return MLA_QCACHE_ERR_NULL;

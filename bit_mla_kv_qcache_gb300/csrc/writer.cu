@@ -3,8 +3,8 @@
 // Per new token (one CTA each): BF16 retention in the sink buffer / recent ring, per-token
 // clip of the latent at a nearest-rank quantile of |c|, per-128-channel-group quantization
 // with an FP16 minimum (rounded down) and FP16 scale (rounded up), and the bit-packed store
-// into the token's page slot. Per page that fills during the call (one CTA each): per-channel
-// quantization of k_R over the page's P tokens, earlier tokens read from the ring.
+// into the token's page slot. Per page that fills during the call (four CTAs, 16 channels each):
+// per-channel quantization of k_R over the page's P tokens, earlier tokens read from the ring.
 //
 // Every code is decided exactly: the nearest level is found from a float estimate and then
 // confirmed against the exact midpoints min + (j + 1/2) * scale, which are formed without
@@ -235,8 +235,20 @@ __device__ void write_token(const WriteParams& p, int r, int (&s_cnt)[2][4]) {
   if (lane == 0 && flags) raise_err(p.err, flags);
 }
 
-// ------------------------------------------------------------------ page fill (one CTA)
-__device__ void fill_page(const WriteParams& p, int b, int f, float* vals, float* stats) {
+// ------------------------------------------------------------------ page fill (four CTAs)
+// A page that fills during the call is quantized by four CTAs, CTA rr taking k_R channels
+// 16rr .. 16rr+15: exactly the channels of region B's fragment blocks (tb, rr) and of their
+// region D entries, so the four write disjoint bytes.
+constexpr int kFillSplit = 4;
+constexpr int kFillCh = kRope / kFillSplit;  // 16
+constexpr int kFillStride = kFillCh + 1;     // row stride of the staged values (floats)
+constexpr int kFillSubsets = 8;              // token subsets reduced in parallel per channel
+
+__host__ __device__ constexpr size_t fill_smem_floats(int P) {
+  return static_cast<size_t>(P) * kFillStride + 2 * kFillSubsets * kFillCh + 3 * kFillCh;
+}
+
+__device__ void fill_page(const WriteParams& p, int b, int f, int rr, float* smem) {
   const int tid = threadIdx.x;
   const int r0 = __ldg(p.cu_new + b), r1 = __ldg(p.cu_new + b + 1);
   const int s0 = __ldg(p.seq_lens + b);
@@ -246,46 +258,81 @@ __device__ void fill_page(const WriteParams& p, int b, int f, float* vals, float
   if ((pg + 1) * p.P > static_cast<int64_t>(s0) + n) return;  // this page does not fill now
   if (pg >= p.max_pages) return;
   const int32_t pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
+  const int P = p.P;
+  float* vals = smem;                                        // [P][kFillStride]
+  float* red = vals + static_cast<size_t>(P) * kFillStride;  // [2][kFillSubsets][kFillCh]
+  float* stats = red + 2 * kFillSubsets * kFillCh;           // [kFillCh][3]
+
+  // gather this CTA's 32 bytes of every token of the page (earlier tokens from the ring, new
+  // ones from the input), all loads of a thread in flight together; the page id is checked
+  // after them (the loads do not depend on it)
+  constexpr int kMaxIt = 128 * 8 / 128;  // at most 128 tokens x 8 words, over 128 threads
+  const int n_items = P * 8;
+  uint32_t w[kMaxIt];
+#pragma unroll
+  for (int it = 0; it < kMaxIt; ++it) {
+    const int i = threadIdx.x + 128 * it;
+    w[it] = 0;
+    if (i < n_items) {
+      const int u = i >> 3, e = i & 7;
+      const int64_t tt = pg * P + u;
+      const uint32_t* src;
+      if (tt < s0)
+        src = reinterpret_cast<const uint32_t*>(p.ring + (static_cast<size_t>(b) * p.W + (tt % p.W)) * kRow + kLatent);
+      else
+        src = reinterpret_cast<const uint32_t*>(p.kr_new + static_cast<size_t>(r0 + (tt - s0)) * kRope);
+      w[it] = __ldg(src + kFillCh / 2 * rr + e);
+    }
+  }
   if (pid < 0 || pid >= p.n_pages) return;
   uint8_t* page = p.pool + static_cast<size_t>(pid) * static_cast<size_t>(p.page_bytes);
-  const int P = p.P;
-
-  // gather the page's k_R values: earlier tokens from the ring, new ones from the input
-  for (int idx = tid; idx < P * 32; idx += blockDim.x) {
-    const int u = idx >> 5, jj = idx & 31;
-    const int64_t tt = pg * P + u;
-    const uint32_t* src;
-    if (tt < s0)
-      src = reinterpret_cast<const uint32_t*>(p.ring + (static_cast<size_t>(b) * p.W + (tt % p.W)) * kRow + kLatent);
-    else
-      src = reinterpret_cast<const uint32_t*>(p.kr_new + static_cast<size_t>(r0 + (tt - s0)) * kRope);
-    const uint32_t w = src[jj];
-    vals[u * 65 + 2 * jj] = bf16_lo(w);
-    vals[u * 65 + 2 * jj + 1] = bf16_hi(w);
+#pragma unroll
+  for (int it = 0; it < kMaxIt; ++it) {
+    const int i = threadIdx.x + 128 * it;
+    if (i < n_items) {
+      const int u = i >> 3, e = i & 7;
+      vals[u * kFillStride + 2 * e] = bf16_lo(w[it]);
+      vals[u * kFillStride + 2 * e + 1] = bf16_hi(w[it]);
+    }
   }
   __syncthreads();
+
+  // per-channel range: eight token subsets per channel, then the eight partial ranges
   int flags = 0;
-  if (tid < kRope) {
-    float lo = vals[tid], hi = vals[tid];
-    bool bad = false;
-    for (int u = 0; u < P; ++u) {
-      const float v = vals[u * 65 + tid];
+  {
+    const int c = tid & (kFillCh - 1), sub = tid >> 4;  // 128 threads = 16 channels x 8 subsets
+    float lo = vals[sub * kFillStride + c], hi = lo;
+    bool bad = !isfinite(lo);
+    for (int u = sub + kFillSubsets; u < P; u += kFillSubsets) {
+      const float v = vals[u * kFillStride + c];
       bad |= !isfinite(v);
       lo = fminf(lo, v);
       hi = fmaxf(hi, v);
     }
+    red[sub * kFillCh + c] = lo;
+    red[(kFillSubsets + sub) * kFillCh + c] = hi;
+    if (__syncthreads_or(bad)) flags |= kErrNonFinite;
+  }
+  if (tid < kFillCh) {
+    float lo = red[tid], hi = red[kFillSubsets * kFillCh + tid];
+#pragma unroll
+    for (int sub = 1; sub < kFillSubsets; ++sub) {
+      lo = fminf(lo, red[sub * kFillCh + tid]);
+      hi = fmaxf(hi, red[(kFillSubsets + sub) * kFillCh + tid]);
+    }
     const QParams qp = make_qparams(lo, hi, 15);
-    flags |= qp.flags | (bad ? kErrNonFinite : 0);
+    flags |= qp.flags;
     stats[3 * tid] = qp.m;
     stats[3 * tid + 1] = qp.s;
     stats[3 * tid + 2] = qp.inv_s;
-    *reinterpret_cast<uint32_t*>(page + static_cast<size_t>(P) * (64 * p.bits_c + 48) + tid * 4) = qp.meta;
+    const int j = kFillCh * rr + tid;
+    *reinterpret_cast<uint32_t*>(page + static_cast<size_t>(P) * (64 * p.bits_c + 48) + j * 4) = qp.meta;
   }
   __syncthreads();
-  // codes, one 32-bit word of region B per iteration
+  // codes: the 32-bit words of region B's fragment blocks (tb, rr), one per iteration
   uint8_t* regb = page + static_cast<size_t>(P) * 64 * p.bits_c;
-  for (int wi = tid; wi < P * 8; wi += blockDim.x) {
-    const int tb = wi >> 7, rr = (wi >> 5) & 3, ln = wi & 31;
+  for (int wi = tid; wi < P * 2; wi += blockDim.x) {
+    const int tb = wi >> 5, ln = wi & 31;
     const int q = ln & 3, g8 = ln >> 2;
     uint32_t word = 0;
 #pragma unroll
@@ -295,13 +342,13 @@ __device__ void fill_page(const WriteParams& p, int b, int f, float* vals, float
 #pragma unroll
         for (int o = 0; o < 2; ++o) {
           const int u = 16 * tb + 8 * nn + g8;
-          const int j = 16 * rr + 8 * h + 2 * q + o;
-          const int c = quant_code(vals[u * 65 + j], stats[3 * j], stats[3 * j + 1], stats[3 * j + 2], 15);
-          word |= static_cast<uint32_t>(c) << (4 * (2 * nn + h + 4 * o));
+          const int c = 8 * h + 2 * q + o;
+          const int code = quant_code(vals[u * kFillStride + c], stats[3 * c], stats[3 * c + 1], stats[3 * c + 2], 15);
+          word |= static_cast<uint32_t>(code) << (4 * (2 * nn + h + 4 * o));
         }
     *reinterpret_cast<uint32_t*>(regb + ((tb * 4 + rr) * 128 + ln * 4)) = word;
   }
-  if (flags) raise_err(p.err, flags);
+  if (flags && tid == 0) raise_err(p.err, flags);
 }
 
 __global__ void __launch_bounds__(128) write_kernel(const WriteParams p) {
@@ -315,9 +362,11 @@ __global__ void __launch_bounds__(128) write_kernel(const WriteParams p) {
     return;
   }
   const int idx = blockIdx.x - p.token_blocks;
-  const int b = idx / p.fill_per_seq, f = idx % p.fill_per_seq;
-  if (b < p.B) fill_page(p, b, f, smem_f, smem_f + p.P * 65);
+  const int per_seq = p.fill_per_seq * kFillSplit;
+  const int b = idx / per_seq, f = (idx % per_seq) / kFillSplit, rr = idx % kFillSplit;
+  if (b < p.B) fill_page(p, b, f, rr, smem_f);
 }
+
 
 __global__ void __launch_bounds__(256) advance_kernel(const int32_t* cu_new, int32_t* seq_lens, int B) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
@@ -332,15 +381,11 @@ cudaError_t launch_advance(const int32_t* cu_new, int32_t* seq_lens, int B, cuda
 }
 
 cudaError_t launch_write(const WriteParams& p, cudaStream_t stream) {
-  const int blocks = p.token_blocks + p.B * p.fill_per_seq;
+  const int64_t blocks = p.token_blocks + static_cast<int64_t>(p.B) * p.fill_per_seq * kFillSplit;
   if (blocks == 0) return cudaSuccess;
-  const size_t smem = p.fill_per_seq > 0 ? (static_cast<size_t>(p.P) * 65 + 3 * kRope) * sizeof(float) : 0;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(write_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
-  write_kernel<<<blocks, 128, smem, stream>>>(p);
+  if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  const size_t smem = p.fill_per_seq > 0 ? fill_smem_floats(p.P) * sizeof(float) : 0;  // <= 10 KB
+  write_kernel<<<static_cast<unsigned>(blocks), 128, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

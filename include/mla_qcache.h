@@ -178,7 +178,8 @@ size_t mla_qcache_workspace_bytes(const mla_qcache_config* cfg, int32_t B, int32
  *   sink_buf   [B][S][576] BF16 (may be NULL when S == 0); recent_buf [B][W][576] BF16.
  *   err_word   device int32 receiving MLA_QCACHE_DEV_* bits (required).
  * Errors: NULL pointer, bad config, B < 1, n_rows < 0, max_new < 1 (with n_rows > 0),
- * max_pages < 1, n_pages < 1, misaligned pool or buffers -> negative status, nothing run.
+ * n_rows + 4 * B * (max_new / P + 1) above 2^31 - 1, max_pages < 1, n_pages < 1, misaligned
+ * pool or buffers -> negative status, nothing run.
  */
 int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows,
                      const uint16_t* c_new, const uint16_t* kr_new, const int32_t* cu_new,

@@ -68,6 +68,9 @@ def test_host_validation_without_gpu(L):
     # bad sizes
     assert lib.mla_qcache_write(ctypes.byref(cfg), 0, 4, p, p, p, p, 1, p, 1, p, 1, p, p, p, None) == -3
     assert lib.mla_qcache_write(ctypes.byref(cfg), 1, 4, p, p, p, p, 0, p, 1, p, 1, p, p, p, None) == -3
+    # more write CTAs than one grid dimension holds (4 per page that may fill, per sequence)
+    assert lib.mla_qcache_write(ctypes.byref(cfg), 1 << 20, 4, p, p, p, p, 1 << 20, p, 1, p, 1, p, p, p,
+                                None) == -3
     # misaligned pool
     assert lib.mla_qcache_write(ctypes.byref(cfg), 1, 4, p, p, p, p, 1, p, 1, ctypes.c_void_p(16 * 1024 + 4), 1,
                                 p, p, p, None) == -4
