@@ -16,6 +16,7 @@ SOURCES = {  # file -> extra flags
     "abi.cu": [],
     "writer.cu": ["-fmad=false"],  # exact rounding decisions: keep every product unfused
     "decode.cu": [],
+    "decode_tc.cu": [],
 }
 
 

@@ -102,7 +102,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ float half_lo(uint32_t w) { return __low2float(*reinterpret_cast<const __half2*>(&w)); }
 __device__ __forceinline__ float half_hi(uint32_t w) { return __high2float(*reinterpret_cast<const __half2*>(&w)); }
 // 2^k as a float, k in [-126, 127]
-__device__ __forceinline__ float pow2i(int k) { return __uint_as_float(static_cast<uint32_t>(k + 127) << 23); }
 // 2^x, relative error below 2^-22 (hardware approximation; subnormal results flush to zero)
 __device__ __forceinline__ float exp2_fast(float x) {
   float y;
@@ -399,20 +398,6 @@ __host__ __device__ constexpr int out_log2w(int cb) {
   return BITS == 4 ? 4 * (cb & 1) : 2 * ((cb & 7) <= 4 ? (cb & 7) : (cb & 7) - 5);
 }
 
-// Largest power-of-two exponent E with max_abs * 2^E < 2^15 (FP16-safe prescale of a query
-// row), kept in [-100, 100]; `range` reports queries too large for the prescale.
-__device__ __forceinline__ int prescale_exponent(float max_abs, bool& range) {
-  if (!(max_abs > 0.f)) return 0;
-  int e = static_cast<int>((__float_as_uint(max_abs) >> 23) & 0xffu) - 127;
-  if (e < -126) e = -126;
-  int E = 14 - e;
-  if (E < -100) {
-    E = -100;
-    range = true;
-  }
-  return E > 100 ? 100 : E;
-}
-
 template <int BITS>
 __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int T, int split, State& st,
                              int32_t& flags) {
@@ -509,8 +494,8 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
     if (range) flags |= kErrRange;
     // Partial scores are kept in units of 2^(24 - E) (the latent products' natural scale);
     // the softmax lane of head 4w + lane/8 multiplies the sum back by that head's factor.
-    inv_f[0] = pow2i(E0 - 24);
-    inv_f[1] = pow2i(E1 - 24);
+    inv_f[0] = pow2_int(E0 - 24);
+    inv_f[1] = pow2_int(E1 - 24);
     qsum[0] *= inv_f[0];
     qsum[1] *= inv_f[1];
     {
@@ -519,14 +504,14 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
 #pragma unroll
       for (int w = 0; w < 4; ++w) mh = fmaxf(mh, sh.qmax[w * 16 + hh]);
       bool r2 = false;
-      head_scale = p.scale_log2 * pow2i(24 - prescale_exponent(mh, r2));
+      head_scale = p.scale_log2 * pow2_int(24 - prescale_exponent(mh, r2));
     }
 #pragma unroll
     for (int kc = 0; kc < 8; ++kc)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int lw = slot_log2w<BITS>(kc, 2 * j);
-        const float s0 = pow2i(E0 - lw), s1 = pow2i(E1 - lw);
+        const float s0 = pow2_int(E0 - lw), s1 = pow2_int(E1 - lw);
         const uint32_t v0 = qa[kc][2 * j], v1 = qa[kc][2 * j + 1];
         qa[kc][2 * j] = pack_f16x2(bf16_lo(v0) * s0, bf16_hi(v0) * s0);
         qa[kc][2 * j + 1] = pack_f16x2(bf16_lo(v1) * s1, bf16_hi(v1) * s1);
@@ -892,7 +877,7 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
   float* tile = reinterpret_cast<float*>(sh.stages);
 #pragma unroll
   for (int cb = 0; cb < 16; ++cb) {
-    const float sc = pow2i(24 - out_log2w<BITS>(cb));
+    const float sc = pow2_int(24 - out_log2w<BITS>(cb));
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int ch = 128 * warp + out_channel<BITS>(cb, 2 * q + c);
@@ -1065,6 +1050,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p) {
 }  // namespace
 
 int decode_num_splits(int B, int H, int max_pages, int P, int num_sms) {
+  if (decode_uses_tc(H)) return decode_tc_num_splits(B, H, max_pages, P, num_sms);
   const int groups = B * (H / 16);
   const int target = kCtasPerSm * num_sms;  // one full wave of resident CTAs
   int ns = target / (groups > 0 ? groups : 1) - 1;
@@ -1089,6 +1075,9 @@ int decode_num_protected(int B, int H, int max_pages, int P, int S, int W, int n
   const long long groups = static_cast<long long>(B) * (H / 16);
   const long long wave = static_cast<long long>(kCtasPerSm) * (num_sms > 0 ? num_sms : 1);
   const long long prot_max = (S > 0 ? 1 : 0) + (W + kTile - 1) / kTile;
+  // 64-head blocks: the protected CTAs run as their own launch ahead of the packed shares, so
+  // each takes one tile (a short launch instead of one long CTA per head block)
+  if (decode_uses_tc(H)) return static_cast<int>(prot_max);
   const long long T = static_cast<long long>(max_pages) * P;
   const long long packed_max = T > S + W ? (T - W - 1) / kPT - S / kPT + 1 : 0;
   if (2 * groups * packed_max >= wave * prot_max) return 1;
@@ -1119,7 +1108,9 @@ cudaError_t ensure_smem_attr() {
 }
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
-  const dim3 grid(p.B, p.H / 16, p.n_q + p.n_split);
+  // 64-head blocks: the packed shares run on the tensor-memory kernel, the protected shares here
+  const bool tc = decode_uses_tc(p.H);
+  const dim3 grid(p.B, p.H / 16, tc ? p.n_q : p.n_q + p.n_split);
   cudaError_t e;
   if (p.bits_c == 4) {
     if ((e = ensure_smem_attr<4>()) != cudaSuccess) return e;
@@ -1130,6 +1121,7 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (tc && (e = launch_decode_tc(p, stream)) != cudaSuccess) return e;
   combine_kernel<<<p.B * p.H, 128, 0, stream>>>(p);
   return cudaGetLastError();
 }

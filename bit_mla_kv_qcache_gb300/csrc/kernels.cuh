@@ -70,6 +70,11 @@ struct DecodeParams {
 int decode_num_splits(int B, int H, int max_pages, int P, int num_sms);
 int decode_num_protected(int B, int H, int max_pages, int P, int S, int W, int num_sms);
 size_t decode_workspace_bytes(int B, int H, int n_slots);  // n_slots = n_split + n_q
+// Head counts that are multiples of 64 run the packed shares on tcgen05 tensor cores (64 heads
+// per CTA, one CTA per SM); the others on the 16-head warp-level kernel.
+inline bool decode_uses_tc(int H) { return H % 64 == 0; }
+int decode_tc_num_splits(int B, int H, int max_pages, int P, int num_sms);
+cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 
 // Built-in decode scratch for callers that cannot allocate (mla_qcache_decode_attn_noalloc).

@@ -117,4 +117,21 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
   return d;
 }
 
+// 2^k as a float for k in [-126, 127]
+__device__ __forceinline__ float pow2_int(int k) { return __uint_as_float(static_cast<uint32_t>(k + 127) << 23); }
+
+// Largest power-of-two exponent E with max_abs * 2^E < 2^15 (FP16-safe prescale of a query
+// row), kept in [-100, 100]; `range` reports queries too large for the prescale.
+__device__ __forceinline__ int prescale_exponent(float max_abs, bool& range) {
+  if (!(max_abs > 0.f)) return 0;
+  int e = static_cast<int>((__float_as_uint(max_abs) >> 23) & 0xffu) - 127;
+  if (e < -126) e = -126;
+  int E = 14 - e;
+  if (E < -100) {
+    E = -100;
+    range = true;
+  }
+  return E > 100 ? 100 : E;
+}
+
 }  // namespace mlaq

@@ -111,3 +111,52 @@ def test_bad_page_sets_error_bit():
     torch.cuda.synchronize()
     assert cache.error_bits() & 1
     assert torch.isfinite(out).all()
+
+
+# ---- 64-head blocks: the packed shares run on the tcgen05 kernel (128-token tiles)
+
+@pytest.mark.parametrize("T", [0, 1, 133, 259, 260, 261, 388, 1000, 2100])
+def test_tc_boundaries_c4(T):
+    _run(C4, [T, max(0, T - 1)], heads=64)
+
+
+@pytest.mark.parametrize("T", [1, 131, 132, 133, 260, 777, 1500])
+def test_tc_boundaries_c2(T):
+    _run(C2, [T, T + 16, 3], heads=64)
+
+
+def test_tc_small_window_small_pages():
+    """A recent window of 32: the last 128-token tile of a share runs past the written
+    positions (those rows are neither loaded nor weighted)."""
+    w = workloads.Workload("s0", 1, 16, 1, 4, 32, n_sink=0, n_recent=32, random_pages=True, seed=5)
+    _run(w, [500, 33, 32, 31, 65, 64, 300], heads=64)
+
+
+def test_tc_wide_window_and_sinks():
+    w = workloads.Workload("s16", 1, 16, 1, 2, 32, n_sink=16, n_recent=256, clip_q=0.94, random_pages=True, seed=6)
+    _run(w, [900, 272, 271, 40, 1200], heads=128)
+
+
+def test_tc_peaked_softmax():
+    """Concentrated weights: the running maximum is raised inside a share."""
+    _run(C4, [1600, 250], heads=64, scale=0.5)
+
+
+def test_tc_many_sequences():
+    rng = np.random.default_rng(9)
+    lens = rng.integers(0, 1300, size=40)
+    lens[::5] = 0
+    lens[::7] = 132
+    _run(C2, lens, heads=64)
+
+
+def test_tc_bad_page_sets_error_bit():
+    inp = workloads.make_inputs(C4, seq_lens=np.array([700], np.int32), heads=64)
+    kw = C4.config_kwargs()
+    cache = gu.gpu_cache(kw, inp)
+    gu.write_rows(cache, inp.c, inp.kr, inp.seq_lens, 700)
+    cache.page_table[0, 2] = 10 ** 6
+    out, lse = cache.decode(gu.dev(inp.q_lat), gu.dev(inp.q_rope), C4.softmax_scale)
+    torch.cuda.synchronize()
+    assert cache.error_bits() & 1
+    assert torch.isfinite(out).all()
