@@ -35,6 +35,7 @@ import workloads  # noqa: E402
 METRIC = "decode attn µs/layer and packed-cache HBM GB/s (fraction of 8 TB/s) on 1 GB300"
 DEFAULT_WORKLOAD = "v2lite_c4r4_b32_h16_t8k"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -92,12 +93,14 @@ def decode_flops(seq_lens, heads) -> int:
 
 
 def peaks():
+    """(HBM GB/s, dense 16-bit tensor TFLOP/s burst, which): the measured copy bandwidth and
+    bf16 GEMM rate of this GPU pool (FP16 and BF16 share the dense tensor rate)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def source_sha() -> str:
@@ -361,9 +364,25 @@ def run_native(args, w):
     mean_T = caches[0].seq_lens.cpu().numpy()
     bytes_dec = decode_bytes(w, mean_T, H)
     flops_dec = decode_flops(mean_T, H)
-    hbm_peak, peak_kind = peaks()
+    hbm_peak, tensor_peak, peak_kind = peaks()
     achieved = bytes_dec / (dec_us * 1e-6) / 1e9
+    tflops = flops_dec / (dec_us * 1e-6) / 1e12
     traffic = profiled_traffic(w.name)
+    if H % 64 == 0:
+        # 64-head blocks run the packed tokens on tcgen05 tensor cores; at ~1000 flops per packed
+        # byte the decode is bound by the tensor pipe, not by HBM
+        roofline = {"bound": "tensor", "achieved": tflops, "peak": tensor_peak, "unit": "TFLOP/s",
+                    "frac": tflops / tensor_peak, "traffic": traffic,
+                    "kernel": "mla_qcache_decode_attn (decode_tc_kernel + protected decode_kernel + combine_kernel)",
+                    "algorithmic_flops_per_call": flops_dec, "algorithmic_bytes_per_call": bytes_dec,
+                    "hbm_frac": achieved / hbm_peak, "peak_kind": peak_kind}
+        launches_per_step = 5  # write, advance, protected decode, tensor-core decode, merge
+    else:
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": achieved / hbm_peak, "traffic": traffic,
+                    "kernel": "mla_qcache_decode_attn (decode_kernel + combine_kernel)",
+                    "algorithmic_bytes_per_call": bytes_dec, "peak_kind": peak_kind}
+        launches_per_step = 4  # write, advance, decode, merge
 
     result = {
         "metric": METRIC, "value": us_step * 1.0, "unit": "us/layer", "n_gpus": ws, "steps": args.steps,
@@ -371,12 +390,9 @@ def run_native(args, w):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(w, NL),
         "decode_us": dec_us, "write_and_advance_us": max(0.0, us_step - dec_us),
         "packed_cache_gbs": achieved, "fraction_of_8tbs": achieved / 8000.0,
-        "decode_tflops": flops_dec / (dec_us * 1e-6) / 1e12,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": traffic,
-                     "kernel": "mla_qcache_decode_attn (decode_kernel + combine_kernel)",
-                     "algorithmic_bytes_per_call": bytes_dec, "peak_kind": peak_kind},
-        "gpu_launches": 4 * args.steps,  # per step: write_kernel, advance_kernel, decode_kernel, combine_kernel
+        "decode_tflops": tflops,
+        "roofline": roofline,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
 
