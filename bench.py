@@ -299,39 +299,52 @@ def run_native(args, w):
     ws_buf = caches[0].workspace(H)
     stream = torch.cuda.Stream(device=dev)
 
-    def write_step(cache):
-        q.mla_qcache_write(cfg, c_new, kr_new, cu1, cache.seq_lens, 1, cache.page_table, cache.pool, cache.sink,
-                           cache.ring, cache.err)
-        q.mla_qcache_advance(cu1, cache.seq_lens)
+    # Each layer keeps two length arrays: a step writes the new token with the lengths of one
+    # and stores the advanced lengths into the other (one launch), then decodes with those.
+    lens_alt = [c.seq_lens.clone() for c in caches]
 
-    def decode_step(cache):
-        q.mla_qcache_decode_attn(cfg, q_lat, q_rope, cache.page_table, cache.seq_lens, cache.pool, cache.sink,
+    def write_step(cache, lens_in, lens_out):
+        q.mla_qcache_write_advance(cfg, c_new, kr_new, cu1, lens_in, lens_out, 1, cache.page_table, cache.pool,
+                                   cache.sink, cache.ring, cache.err)
+
+    def decode_step(cache, lens):
+        q.mla_qcache_decode_attn(cfg, q_lat, q_rope, cache.page_table, lens, cache.pool, cache.sink,
                                  cache.ring, w.softmax_scale, out, lse, ws_buf, cache.err)
 
-    # One CUDA graph per layer-step (write + length advance + decode): the timed region replays
-    # exactly K of them. A second live pass replays decode-only graphs with CUDA events around
-    # each call to measure the decode kernels for the roofline.
+    # Two CUDA graphs per layer (write + decode, lengths A -> B and B -> A) replayed alternately:
+    # the timed region replays exactly K of them. A second live pass replays decode-only graphs
+    # with CUDA events around each call to measure the decode kernels for the roofline.
     g_step, g_dec = [], []
     with torch.cuda.stream(stream):
         for cache in caches:  # warm the code paths once before capture
-            decode_step(cache)
+            decode_step(cache, cache.seq_lens)
         torch.cuda.synchronize()
-        for cache in caches:
-            gs, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gs, stream=stream):
-                write_step(cache)
-                decode_step(cache)
+        for cache, alt in zip(caches, lens_alt):
+            pair = []
+            for lens_in, lens_out in ((cache.seq_lens, alt), (alt, cache.seq_lens)):
+                gs = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gs, stream=stream):
+                    write_step(cache, lens_in, lens_out)
+                    decode_step(cache, lens_out)
+                pair.append(gs)
+            gd = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gd, stream=stream):
-                decode_step(cache)
-            g_step.append(gs)
+                decode_step(cache, cache.seq_lens)
+            g_step.append(pair)
             g_dec.append(gd)
     torch.cuda.synchronize()
+    uses = [0] * NL
+
+    def replay_step(k):
+        layer = k % NL
+        g_step[layer][uses[layer] & 1].replay()
+        uses[layer] += 1
 
     head_start = torch.empty(int(1.5e9) // 4, dtype=torch.float32, device=dev)  # lets the host queue ahead
 
     with torch.cuda.stream(stream):
         for k in range(args.warmup):
-            g_step[k % NL].replay()
+            replay_step(k)
         torch.cuda.synchronize()
         if ws > 1:
             torch.distributed.barrier()
@@ -340,7 +353,7 @@ def run_native(args, w):
             head_start.fill_(1.0)
             start.record(stream)
             for k in range(args.steps):
-                g_step[k % NL].replay()
+                replay_step(args.warmup + k)
             end.record(stream)
             torch.cuda.synchronize()
         total_ms = start.elapsed_time(end)
@@ -361,7 +374,7 @@ def run_native(args, w):
     us_step = total_ms * 1e3 / args.steps
     dec_us = statistics.mean(dec_ms) * 1e3
     # sequence lengths seen by the decode-only pass (after the timed steps)
-    mean_T = caches[0].seq_lens.cpu().numpy()
+    mean_T = np.maximum(caches[0].seq_lens.cpu().numpy(), lens_alt[0].cpu().numpy())  # the newer of the two
     bytes_dec = decode_bytes(w, mean_T, H)
     flops_dec = decode_flops(mean_T, H)
     hbm_peak, tensor_peak, peak_kind = peaks()
@@ -376,13 +389,13 @@ def run_native(args, w):
                     "kernel": "mla_qcache_decode_attn (decode_tc_kernel + protected decode_kernel + combine_kernel)",
                     "algorithmic_flops_per_call": flops_dec, "algorithmic_bytes_per_call": bytes_dec,
                     "hbm_frac": achieved / hbm_peak, "peak_kind": peak_kind}
-        launches_per_step = 5  # write, advance, protected decode, tensor-core decode, merge
+        launches_per_step = 4  # fused write + length update, protected decode, tensor-core decode, merge
     else:
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                     "frac": achieved / hbm_peak, "traffic": traffic,
                     "kernel": "mla_qcache_decode_attn (decode_kernel + combine_kernel)",
                     "algorithmic_bytes_per_call": bytes_dec, "peak_kind": peak_kind}
-        launches_per_step = 4  # write, advance, decode, merge
+        launches_per_step = 3  # fused write + length update, decode, merge
 
     result = {
         "metric": METRIC, "value": us_step * 1.0, "unit": "us/layer", "n_gpus": ws, "steps": args.steps,
@@ -430,7 +443,7 @@ def e2e_measure(args, w, q, cache, cfg, inp, dev):
         d_k.copy_(h_k, non_blocking=True)
         d_ql.copy_(h_ql, non_blocking=True)
         d_qr.copy_(h_qr, non_blocking=True)
-        cache.write(d_c, d_k, cu1, 1)
+        cache.write_advance(d_c, d_k, cu1, 1)
         cache.decode(d_ql, d_qr, w.softmax_scale, out=out, lse=lse)
         h_out.copy_(out, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)

@@ -6,9 +6,9 @@ buffers (pool, BF16 sink/recent buffers, workspace) of one layer.
 """
 from .binding import (DEV_BAD_PAGE, DEV_NONFINITE, DEV_RANGE, DEV_ROWS, DEV_SEQ_OVERFLOW, DEV_TIMEOUT, EXPORTS,
                       Config, QCacheError, lib, make_config, mla_qcache_advance, mla_qcache_decode_attn,
-                      mla_qcache_write, page_bytes, strerror, workspace_bytes)
+                      mla_qcache_write, mla_qcache_write_advance, page_bytes, strerror, workspace_bytes)
 from .cache import QuantizedMLACache
 
 __all__ = ["Config", "QCacheError", "QuantizedMLACache", "lib", "make_config", "mla_qcache_advance", "mla_qcache_decode_attn",
-           "mla_qcache_write", "page_bytes", "strerror", "workspace_bytes", "EXPORTS", "DEV_BAD_PAGE",
+           "mla_qcache_write", "mla_qcache_write_advance", "page_bytes", "strerror", "workspace_bytes", "EXPORTS", "DEV_BAD_PAGE",
            "DEV_NONFINITE", "DEV_RANGE", "DEV_ROWS", "DEV_SEQ_OVERFLOW", "DEV_TIMEOUT"]

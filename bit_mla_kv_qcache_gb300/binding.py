@@ -20,7 +20,8 @@ DEV_BAD_PAGE, DEV_SEQ_OVERFLOW, DEV_NONFINITE, DEV_RANGE, DEV_ROWS, DEV_TIMEOUT 
 # the entry points declared in include/mla_qcache.h
 EXPORTS = ("mla_qcache_page_bytes", "mla_qcache_config_check", "mla_qcache_workspace_bytes",
            "mla_qcache_write", "mla_qcache_decode_attn", "mla_qcache_strerror",
-           "mla_qcache_decode_attn_noalloc", "mla_qcache_noalloc_scratch_bytes", "mla_qcache_advance")
+           "mla_qcache_decode_attn_noalloc", "mla_qcache_noalloc_scratch_bytes", "mla_qcache_advance",
+           "mla_qcache_write_advance")
 
 
 class Config(ctypes.Structure):
@@ -71,6 +72,9 @@ def lib() -> ctypes.CDLL:
                                                      ctypes.c_float, vp, vp, vp, vp]
         L.mla_qcache_noalloc_scratch_bytes.restype = sz
         L.mla_qcache_noalloc_scratch_bytes.argtypes = []
+        L.mla_qcache_write_advance.restype = ctypes.c_int
+        L.mla_qcache_write_advance.argtypes = [P(Config), i32, i32, vp, vp, vp, vp, vp, i32, vp, i32, vp, i64, vp, vp,
+                                               vp, vp]
         L.mla_qcache_advance.restype = ctypes.c_int
         L.mla_qcache_advance.argtypes = [vp, vp, i32, vp]
         L.mla_qcache_strerror.restype = ctypes.c_char_p
@@ -130,6 +134,22 @@ def mla_qcache_write(cfg: Config, c_new, kr_new, cu_new, seq_lens, max_new: int,
         pool.shape[0], _ptr(sink_buf, "sink_buf", 2, allow_none=True) if cfg.n_sink else None,
         _ptr(recent_buf, "recent_buf", 2), _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
     _raise(st, "mla_qcache_write")
+
+
+def mla_qcache_write_advance(cfg: Config, c_new, kr_new, cu_new, seq_lens, seq_lens_next, max_new: int,
+                             page_table, pool, sink_buf, recent_buf, err_word, stream=None) -> None:
+    """mla_qcache_write plus seq_lens_next = seq_lens + rows per sequence in the same launch
+    (see include/mla_qcache.h); seq_lens_next must be a separate int32 array."""
+    B = seq_lens.shape[0]
+    n_rows = c_new.shape[0]
+    st = lib().mla_qcache_write_advance(
+        ctypes.byref(cfg), B, n_rows, _ptr(c_new, "c_new", 2), _ptr(kr_new, "kr_new", 2),
+        _ptr(cu_new, "cu_new", dtype=torch.int32), _ptr(seq_lens, "seq_lens", dtype=torch.int32),
+        _ptr(seq_lens_next, "seq_lens_next", dtype=torch.int32), int(max_new),
+        _ptr(page_table, "page_table", dtype=torch.int32), page_table.shape[1], _ptr(pool, "pool", 1),
+        pool.shape[0], _ptr(sink_buf, "sink_buf", 2, allow_none=True) if cfg.n_sink else None,
+        _ptr(recent_buf, "recent_buf", 2), _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
+    _raise(st, "mla_qcache_write_advance")
 
 
 def mla_qcache_advance(cu_new, seq_lens, stream=None) -> None:

@@ -37,6 +37,7 @@ class QuantizedMLACache:
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self._ws = None
         self._ws_need = {}  # workspace bytes per head count
+        self._lens_alt = None  # second length array for write_advance
 
     def write(self, c_new: torch.Tensor, kr_new: torch.Tensor, cu_new: torch.Tensor, max_new: int,
               advance: bool = True, stream=None) -> None:
@@ -45,6 +46,16 @@ class QuantizedMLACache:
                                  self.sink, self.ring, self.err, stream)
         if advance:
             binding.mla_qcache_advance(cu_new, self.seq_lens, stream)
+
+    def write_advance(self, c_new: torch.Tensor, kr_new: torch.Tensor, cu_new: torch.Tensor, max_new: int,
+                      stream=None) -> None:
+        """write() with the length update in the same launch: the new lengths are stored into a
+        second array, which then becomes ``self.seq_lens`` (the two arrays alternate)."""
+        if self._lens_alt is None:
+            self._lens_alt = torch.empty_like(self.seq_lens)
+        binding.mla_qcache_write_advance(self.cfg, c_new, kr_new, cu_new, self.seq_lens, self._lens_alt, max_new,
+                                         self.page_table, self.pool, self.sink, self.ring, self.err, stream)
+        self.seq_lens, self._lens_alt = self._lens_alt, self.seq_lens
 
     def workspace(self, heads: int) -> torch.Tensor:
         need = self._ws_need.get(heads)

@@ -55,14 +55,24 @@ size_t mla_qcache_workspace_bytes(const mla_qcache_config* cfg, int32_t B, int32
   return mlaq::decode_workspace_bytes(B, H, ns + nq);
 }
 
-int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, const uint16_t* c_new,
+}  // extern "C"
+
+static int write_impl(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, const uint16_t* c_new,
                      const uint16_t* kr_new, const int32_t* cu_new, const int32_t* seq_lens, int32_t max_new,
                      const int32_t* page_table, int32_t max_pages, uint8_t* pool, int64_t n_pages,
-                     uint16_t* sink_buf, uint16_t* recent_buf, int32_t* err_word, void* stream) {
+                     uint16_t* sink_buf, uint16_t* recent_buf, int32_t* err_word, int32_t* seq_next, void* stream) {
   int st = check_config(cfg);
   if (st != MLA_QCACHE_OK) return st;
   if (B < 1 || B > (1 << 20) || n_rows < 0 || max_pages < 1 || n_pages < 1) return MLA_QCACHE_ERR_SHAPE;
-  if (n_rows == 0) return MLA_QCACHE_OK;
+  if (n_rows == 0) {  // nothing to write; the next lengths equal the current ones
+    if (seq_next == nullptr) return MLA_QCACHE_OK;
+    if (!seq_lens) return MLA_QCACHE_ERR_NULL;
+    if (!aligned(seq_lens, 4) || !aligned(seq_next, 4)) return MLA_QCACHE_ERR_ALIGN;
+    return cudaMemcpyAsync(seq_next, seq_lens, static_cast<size_t>(B) * sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                           static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MLA_QCACHE_OK
+               : MLA_QCACHE_ERR_CUDA;
+  }
   if (max_new < 1) return MLA_QCACHE_ERR_SHAPE;
   // one CTA per row plus four per page that may fill, in one grid dimension
   if (static_cast<int64_t>(B) * (max_new / cfg->page_size + 1) * 4 + n_rows > 0x7fffffff)
@@ -72,7 +82,7 @@ int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, co
   if (cfg->n_sink > 0 && !sink_buf) return MLA_QCACHE_ERR_NULL;
   if (!aligned(c_new, 16) || !aligned(kr_new, 4) || !aligned(pool, 16) || !aligned(recent_buf, 16) ||
       (sink_buf && !aligned(sink_buf, 16)) || !aligned(cu_new, 4) || !aligned(seq_lens, 4) ||
-      !aligned(page_table, 4) || !aligned(err_word, 4))
+      !aligned(page_table, 4) || !aligned(err_word, 4) || (seq_next && !aligned(seq_next, 4)))
     return MLA_QCACHE_ERR_ALIGN;
 
   mlaq::WriteParams p{};
@@ -100,6 +110,7 @@ int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, co
   p.sink = sink_buf;
   p.ring = recent_buf;
   p.err = err_word;
+  p.seq_next = seq_next;
   const int token_blocks = n_rows;  // one CTA per new token
   const int fill_per_seq = max_new / p.P + 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -117,10 +128,36 @@ int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, co
     if (e == cudaSuccess) {
       p.token_blocks = token_blocks;
       p.fill_per_seq = 0;
+      p.seq_next = nullptr;  // written by the first launch
       e = mlaq::launch_write(p, s);
     }
   }
   return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
+}
+
+extern "C" {
+
+int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, const uint16_t* c_new,
+                     const uint16_t* kr_new, const int32_t* cu_new, const int32_t* seq_lens, int32_t max_new,
+                     const int32_t* page_table, int32_t max_pages, uint8_t* pool, int64_t n_pages,
+                     uint16_t* sink_buf, uint16_t* recent_buf, int32_t* err_word, void* stream) {
+  return write_impl(cfg, B, n_rows, c_new, kr_new, cu_new, seq_lens, max_new, page_table, max_pages, pool, n_pages,
+                    sink_buf, recent_buf, err_word, nullptr, stream);
+}
+
+int mla_qcache_write_advance(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, const uint16_t* c_new,
+                             const uint16_t* kr_new, const int32_t* cu_new, const int32_t* seq_lens,
+                             int32_t* seq_lens_next, int32_t max_new, const int32_t* page_table, int32_t max_pages,
+                             uint8_t* pool, int64_t n_pages, uint16_t* sink_buf, uint16_t* recent_buf,
+                             int32_t* err_word, void* stream) {
+  if (!seq_lens_next) return MLA_QCACHE_ERR_NULL;
+  if (B >= 1 && seq_lens) {  // the two length arrays must not overlap
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(seq_lens), b0 = reinterpret_cast<uintptr_t>(seq_lens_next);
+    const uintptr_t len = static_cast<uintptr_t>(B) * sizeof(int32_t);
+    if (a0 < b0 + len && b0 < a0 + len) return MLA_QCACHE_ERR_SHAPE;
+  }
+  return write_impl(cfg, B, n_rows, c_new, kr_new, cu_new, seq_lens, max_new, page_table, max_pages, pool, n_pages,
+                    sink_buf, recent_buf, err_word, seq_lens_next, stream);
 }
 
 int mla_qcache_advance(const int32_t* cu_new, int32_t* seq_lens, int32_t B, void* stream) {

@@ -34,6 +34,7 @@ struct WriteParams {
   uint16_t* sink;
   uint16_t* ring;
   int32_t* err;
+  int32_t* seq_next;  // optional: lengths after the call (written by page-fill CTA 0 of each sequence)
   int token_blocks;  // blocks [0, token_blocks) do per-token work (one token per block)
   int fill_per_seq;  // page-fill blocks per sequence after the token blocks
 };

@@ -253,6 +253,8 @@ __device__ void fill_page(const WriteParams& p, int b, int f, int rr, float* sme
   const int r0 = __ldg(p.cu_new + b), r1 = __ldg(p.cu_new + b + 1);
   const int s0 = __ldg(p.seq_lens + b);
   const int n = r1 - r0;
+  // the length after this call, into a second array (the token and fill CTAs read seq_lens)
+  if (p.seq_next != nullptr && f == 0 && rr == 0 && tid == 0) p.seq_next[b] = s0 + n;
   if (s0 < 0 || n <= 0 || n > p.max_new || r0 < 0 || r1 > p.n_rows) return;  // reported by the token work
   const int64_t pg = static_cast<int64_t>(s0) / p.P + f;
   if ((pg + 1) * p.P > static_cast<int64_t>(s0) + n) return;  // this page does not fill now

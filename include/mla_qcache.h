@@ -188,6 +188,23 @@ int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows,
                      uint16_t* recent_buf, int32_t* err_word, void* stream);
 
 /*
+ * Fused cache writer with the length update: exactly mla_qcache_write, and in the same launch
+ * seq_lens_next[b] = seq_lens[b] + cu_new[b+1] - cu_new[b] for every b in [0, B) (a decode
+ * step then needs no separate length kernel). seq_lens_next [B] is a device int32 array,
+ * 4-byte aligned, that must not overlap seq_lens (the writer's CTAs read seq_lens while the
+ * new lengths are stored); callers alternate two length arrays from step to step. With
+ * n_rows == 0 the lengths are copied on `stream`.
+ * Errors: those of mla_qcache_write; seq_lens_next NULL -> MLA_QCACHE_ERR_NULL; overlapping
+ * seq_lens -> MLA_QCACHE_ERR_SHAPE; misaligned -> MLA_QCACHE_ERR_ALIGN.
+ */
+int mla_qcache_write_advance(const mla_qcache_config* cfg, int32_t B, int32_t n_rows,
+                             const uint16_t* c_new, const uint16_t* kr_new, const int32_t* cu_new,
+                             const int32_t* seq_lens, int32_t* seq_lens_next, int32_t max_new,
+                             const int32_t* page_table, int32_t max_pages, uint8_t* pool,
+                             int64_t n_pages, uint16_t* sink_buf, uint16_t* recent_buf,
+                             int32_t* err_word, void* stream);
+
+/*
  * Length update after a write (the pages leave the bookkeeping to the caller): for every
  * sequence b in [0, B), seq_lens[b] += cu_new[b+1] - cu_new[b], in one kernel on `stream`,
  * ordered after a preceding mla_qcache_write on the same stream. cu_new [B+1] and seq_lens [B]

@@ -88,6 +88,16 @@ def test_host_validation_without_gpu(L):
     assert lib.mla_qcache_advance(p, None, 4, None) == -1
     assert lib.mla_qcache_advance(p, p, 0, None) == -3
     assert lib.mla_qcache_advance(ctypes.c_void_p(16 * 1024 + 2), p, 4, None) == -4
+    # fused write + length update: a second, non-overlapping, aligned length array is required
+    p2 = ctypes.c_void_p(32 * 1024)
+    args = lambda lens, nxt: (ctypes.byref(cfg), 4, 4, p, p, p, lens, nxt, 1, p, 1, p, 1, p, p, p, None)
+    assert lib.mla_qcache_write_advance(*args(p, None)) == -1
+    assert lib.mla_qcache_write_advance(*args(p, p)) == -3
+    assert lib.mla_qcache_write_advance(*args(p, ctypes.c_void_p(16 * 1024 + 8))) == -3  # overlaps [p, p+16)
+    assert lib.mla_qcache_write_advance(*args(p, ctypes.c_void_p(32 * 1024 + 2))) == -4
+    # the write's own checks still apply (bad config)
+    assert lib.mla_qcache_write_advance(ctypes.byref(L.make_config(4, 128, n_recent=64)), 4, 4, p, p, p, p, p2, 1, p,
+                                        1, p, 1, p, p, p, None) == -2
 
 
 def test_product_path_has_no_cpu_fallback(L, monkeypatch):

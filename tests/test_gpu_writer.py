@@ -129,3 +129,48 @@ def test_advance_lengths():
     q.mla_qcache_advance(cu, lens)
     torch.cuda.synchronize()
     assert lens.cpu().tolist() == [1, 5, 133, 13, (1 << 20) + 1]
+
+
+@pytest.mark.parametrize("bits_c,P,S,W,lens", [(4, 128, 4, 128, [1, 5, 127, 128, 129, 300]),
+                                              (2, 64, 4, 128, [64, 63, 700, 131]),
+                                              (2, 32, 0, 32, [65, 33, 32, 0])])
+def test_write_advance_equals_write_then_advance(bits_c, P, S, W, lens):
+    """The fused entry stores the same cache bytes as mla_qcache_write and the lengths that
+    mla_qcache_advance would produce, into the second length array (prefill, then decode steps
+    that cross page fills, and a call without rows)."""
+    import bit_mla_kv_qcache_gb300 as q
+    w = _wl(bits_c, P, S, W)
+    lens = np.array(lens, np.int32)
+    inp = workloads.make_inputs(w, seq_lens=lens, extra_pages=3)
+    kw = w.config_kwargs()
+    a, b = gu.gpu_cache(kw, inp), gu.gpu_cache(kw, inp)
+    c, kr, cu = gu.dev(inp.c), gu.dev(inp.kr), gu.dev(inp.cu)
+    mx = max(1, int(lens.max()))
+    a.write(c, kr, cu, mx)  # write + advance
+    nxt = torch.full_like(b.seq_lens, -7)
+    q.mla_qcache_write_advance(b.cfg, c, kr, cu, b.seq_lens, nxt, mx, b.page_table, b.pool, b.sink, b.ring, b.err)
+    torch.cuda.synchronize()
+    assert torch.equal(a.pool, b.pool) and torch.equal(a.sink, b.sink) and torch.equal(a.ring, b.ring)
+    assert torch.equal(b.seq_lens.cpu(), torch.zeros(len(lens), dtype=torch.int32))  # input lengths untouched
+    assert nxt.cpu().tolist() == a.seq_lens.cpu().tolist() == lens.tolist()
+    rng = np.random.default_rng(4)
+    cur, alt = nxt, b.seq_lens
+    B = len(lens)
+    cu1 = torch.arange(B + 1, dtype=torch.int32, device="cuda")
+    for step in range(P + 3):
+        c1, k1 = workloads.draw_tokens(rng, B, w.latent_dist, inp.outliers, w.outlier_scale)
+        d_c, d_k = gu.dev(c1), gu.dev(k1)
+        a.write(d_c, d_k, cu1, 1)
+        q.mla_qcache_write_advance(b.cfg, d_c, d_k, cu1, cur, alt, 1, b.page_table, b.pool, b.sink, b.ring, b.err)
+        cur, alt = alt, cur
+    torch.cuda.synchronize()
+    assert torch.equal(a.pool, b.pool) and torch.equal(a.sink, b.sink) and torch.equal(a.ring, b.ring)
+    assert cur.cpu().tolist() == a.seq_lens.cpu().tolist()
+    # no rows: the lengths are copied
+    empty_c = torch.zeros((0, 512), dtype=torch.int16, device="cuda")
+    empty_k = torch.zeros((0, 64), dtype=torch.int16, device="cuda")
+    q.mla_qcache_write_advance(b.cfg, empty_c, empty_k, torch.zeros(B + 1, dtype=torch.int32, device="cuda"),
+                               cur, alt, 1, b.page_table, b.pool, b.sink, b.ring, b.err)
+    torch.cuda.synchronize()
+    assert alt.cpu().tolist() == cur.cpu().tolist()
+    assert a.error_bits() == 0 and b.error_bits() == 0
