@@ -55,8 +55,9 @@ def test_tiny_workload_full():
     _run(w, [w.seq_len])
 
 
-@pytest.mark.parametrize("heads", [32, 128])
+@pytest.mark.parametrize("heads", [32, 80, 128, 192])
 def test_more_heads(heads):
+    """16-head blocks (32, 80) and 64-head blocks on the tensor-memory kernel (128, 192)."""
     _run(C4, [700, 300], heads=heads)
 
 

@@ -15,11 +15,13 @@ from tests import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 
-def test_noalloc_matches_workspace_entry_point_twice():
+@pytest.mark.parametrize("heads", [16, 64])
+def test_noalloc_matches_workspace_entry_point_twice(heads):
+    """16 heads run the warp-level kernel, 64 the tensor-memory kernel (both share the scratch)."""
     import bit_mla_kv_qcache_gb300 as q
     from bit_mla_kv_qcache_gb300 import binding as b
     w = workloads.Workload("na", 1, 16, 1, 4, 128, random_pages=True, seed=31)
-    inp = workloads.make_inputs(w, seq_lens=np.array([1500, 700, 133, 9], np.int32))
+    inp = workloads.make_inputs(w, seq_lens=np.array([1500, 700, 133, 9], np.int32), heads=heads)
     kw = w.config_kwargs()
     cache = gu.gpu_cache(kw, inp)
     gu.write_rows(cache, inp.c, inp.kr, inp.seq_lens, int(inp.seq_lens.max()))
@@ -27,7 +29,7 @@ def test_noalloc_matches_workspace_entry_point_twice():
     ref_o, ref_l = cache.decode(ql, qr, w.softmax_scale)
     torch.cuda.synchronize()
     ref = (ref_o.cpu().double().numpy(), ref_l.cpu().double().numpy())
-    assert b.noalloc_scratch_bytes() >= b.workspace_bytes(cache.cfg, 4, 16, inp.page_table.shape[1])
+    assert b.noalloc_scratch_bytes() >= b.workspace_bytes(cache.cfg, 4, heads, inp.page_table.shape[1])
     for _ in range(2):  # the scratch keeps the previous call's contents; both calls must agree
         out = torch.full_like(ref_o, float("nan"))
         lse = torch.full_like(ref_l, float("nan"))
