@@ -410,7 +410,7 @@ def run_native(args, w):
     }
 
     if not args.no_e2e:
-        result["e2e"] = e2e_measure(args, w, q, caches[0], cfg, inp, dev)
+        result["e2e"] = e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:
@@ -420,12 +420,16 @@ def run_native(args, w):
     return 0
 
 
-def e2e_measure(args, w, q, cache, cfg, inp, dev):
-    """Same step through the public API from pinned host memory: one H2D copy of the step's new
-    tokens and queries (staged contiguously, as a serving loop would), the fused write and the
-    decode, one D2H copy of O and LSE, all inside the timed region."""
+def e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream):
+    """The step end to end through the public API: every step copies its new tokens and queries
+    from pinned host memory to the device (one copy: staged contiguously, as a serving loop
+    would), runs the fused write and the decode on the same rotated layer caches as the timed
+    steps, and copies O and LSE back to pinned host memory (one copy). Each layer's step (copy
+    in, write, decode, copy out) is captured once as a CUDA graph, as a serving loop drives a
+    decode step, and replayed."""
     import torch
     B, H = w.batch, w.heads
+    NL = len(caches)
     rng = np.random.default_rng(99)
     c1, k1 = workloads.draw_tokens(rng, B, w.latent_dist, inp.outliers, w.outlier_scale)
     parts = [np.ascontiguousarray(a).view(np.int16).reshape(-1) for a in (c1, k1, inp.q_lat, inp.q_rope)]
@@ -442,28 +446,51 @@ def e2e_measure(args, w, q, cache, cfg, inp, dev):
     out, lse = d_res[:n_out].view(B, H, 512), d_res[n_out:].view(B, H)
     h_res = torch.empty_like(d_res, device="cpu").pin_memory()
     cu1 = torch.arange(B + 1, dtype=torch.int32, device=dev)
-    K = max(10, args.steps // 2)
+    ws_buf = caches[0].workspace(H)
 
-    def step():
+    def step(cache, lens_in, lens_out):
         d_in.copy_(h_in, non_blocking=True)
-        cache.write_advance(d_c, d_k, cu1, 1)
-        cache.decode(d_ql, d_qr, w.softmax_scale, out=out, lse=lse)
+        q.mla_qcache_write_advance(cfg, d_c, d_k, cu1, lens_in, lens_out, 1, cache.page_table, cache.pool,
+                                   cache.sink, cache.ring, cache.err)
+        q.mla_qcache_decode_attn(cfg, d_ql, d_qr, cache.page_table, lens_out, cache.pool, cache.sink, cache.ring,
+                                 w.softmax_scale, out, lse, ws_buf, cache.err)
         h_res.copy_(d_res, non_blocking=True)
 
-    for _ in range(3):
-        step()
+    graphs = []
+    with torch.cuda.stream(stream):
+        for cache, alt in zip(caches, lens_alt):
+            pair = []
+            for lens_in, lens_out in ((cache.seq_lens, alt), (alt, cache.seq_lens)):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    step(cache, lens_in, lens_out)
+                pair.append(g)
+            graphs.append(pair)
     torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(K):
-        step()
-    e.record()
-    torch.cuda.synchronize()
+    K = max(10, args.steps // 2)
+    k0 = sum(uses)
+
+    def replay(k):
+        layer = k % NL
+        graphs[layer][uses[layer] & 1].replay()
+        uses[layer] += 1
+
+    with torch.cuda.stream(stream):
+        for k in range(3):
+            replay(k0 + k)
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for k in range(K):
+            replay(k0 + 3 + k)
+        e.record(stream)
+        torch.cuda.synchronize()
     us = s.elapsed_time(e) * 1e3 / K
     h2d = h_in.numel() * h_in.element_size()
     d2h = h_res.numel() * h_res.element_size()
     return {"value": us, "unit": "us/layer", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
-            "note": "eager calls through the Python binding of the C ABI, one layer cache, one H2D and one D2H copy"}
+            "note": "public C ABI calls (fused write, decode) and one H2D + one D2H copy per step, captured per "
+                    "layer as CUDA graphs, layer caches rotated as in the timed steps"}
 
 
 def cpu_baseline(w):
