@@ -220,6 +220,7 @@ int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H, c
   p.bits_c = cfg->bits_c;
   p.n_split = ns;
   p.n_q = nq;
+  p.share_slots = mlaq::decode_share_slots(B, H, max_pages, cfg->page_size, ns, nq, sms);
   const cudaError_t e = mlaq::launch_decode(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
 }

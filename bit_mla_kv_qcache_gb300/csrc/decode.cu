@@ -398,7 +398,7 @@ __host__ __device__ constexpr int out_log2w(int cb) {
   return BITS == 4 ? 4 * (cb & 1) : 2 * ((cb & 7) <= 4 ? (cb & 7) : (cb & 7) - 5);
 }
 
-template <int BITS>
+template <int BITS, bool kBalanced>
 __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int T, int split, State& st,
                              int32_t& flags) {
   using G = Geom<BITS>;
@@ -406,13 +406,49 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
   const int h0 = blockIdx.y * 16;
   const int lo = p.S, hi = T - p.W;
+  // Equal shares sized for one balanced wave over the whole batch: every packed CTA sums the
+  // packed tiles of all sequences (one length per thread) and takes shares of
+  // ceil(total x head blocks / slots) tiles, never fewer than an even split of the longest
+  // table over the launched shares; shares beyond a sequence's end are empty.
+  int share = 0;
+  if constexpr (kBalanced) {
+    long long sum = 0;
+    const long long t_max = static_cast<long long>(p.max_pages) * p.P;
+    for (int bb = threadIdx.x; bb < p.B; bb += kThreads) {
+      long long Tb = __ldg(p.seq_lens + bb);
+      if (Tb < 0 || Tb > t_max) Tb = 0;
+      const long long l2 = p.S, h2 = Tb - p.W;
+      if (h2 > l2) sum += (h2 - 1) / kPT - l2 / kPT + 1;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    long long* red = reinterpret_cast<long long*>(sh.qmax);
+    if (lane == 0) red[warp] = sum;
+    __syncthreads();
+    sum = red[0] + red[1] + red[2] + red[3];
+    __syncthreads();  // the scratch is reused below
+    const long long units = sum * (p.H / 16);
+    const long long by_sum = (units + p.share_slots - 1) / p.share_slots;
+    const long long max_sub = (static_cast<long long>(p.max_pages) * p.P + kPT - 1) / kPT;
+    const long long floor_share = (max_sub + p.n_split - 1) / p.n_split;
+    share = static_cast<int>(by_sum > floor_share ? by_sum : floor_share);
+  }
   int tile_begin = 0, n_my = 0;
   if (hi > lo) {
     const int first = lo / kPT, last = (hi - 1) / kPT;
-    const int n_total = last - first + 1;
-    tile_begin = first + static_cast<int>((static_cast<long long>(n_total) * split) / p.n_split);
-    const int tile_end = first + static_cast<int>((static_cast<long long>(n_total) * (split + 1)) / p.n_split);
-    n_my = tile_end - tile_begin;
+    if (share > 0) {
+      const long long b0 = first + static_cast<long long>(split) * share;
+      const long long e0 = b0 + share < last + 1 ? b0 + share : last + 1;
+      if (e0 > b0) {
+        tile_begin = static_cast<int>(b0);
+        n_my = static_cast<int>(e0 - b0);
+      }
+    } else {  // one wave: an even slice of this sequence's tiles
+      const int n_total = last - first + 1;
+      tile_begin = first + static_cast<int>((static_cast<long long>(n_total) * split) / p.n_split);
+      const int tile_end = first + static_cast<int>((static_cast<long long>(n_total) * (split + 1)) / p.n_split);
+      n_my = tile_end - tile_begin;
+    }
   }
   if (n_my == 0) return;  // empty share (a short sequence): the merge sees sum 0 and skips it
   const int pg0 = (tile_begin * kPT) >> p.p_shift;
@@ -934,7 +970,9 @@ __device__ void protected_split(const DecodeParams& p, const Shared& sh, int b, 
   }
 }
 
-template <int BITS>
+// kBalanced: equal shares sized from the whole batch (launched when more shares than one wave
+// are needed); a separate instance, so the one-wave kernel carries none of its code.
+template <int BITS, bool kBalanced>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const Shared sh = carve<BITS>(smem);
@@ -974,7 +1012,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
   st.l_part = 0.f;
 
   if (is_bf16) protected_split(p, sh, b, T, split - p.n_split, st, flags);
-  else packed_split<BITS>(p, sh, b, T, split, st, flags);
+  else packed_split<BITS, kBalanced>(p, sh, b, T, split, st, flags);
 
   const int NS = p.n_split + p.n_q;
   float l_run = st.l_part;
@@ -1019,11 +1057,12 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (m != -INFINITY && l > 0.f) {
     for (int s0 = 0; s0 < NS; s0 += kBatch) {
-      if (s0 > 0) {
+      if (s0 > 0) {  // rows of empty shares (weight 0) are not loaded
 #pragma unroll
         for (int u = 0; u < kBatch; ++u)
-          v[u] = s0 + u < NS ? *reinterpret_cast<const float4*>(op + static_cast<size_t>(s0 + u) * kLatent)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[u] = s0 + u < NS && (p.share_slots == 0 || ml[2 * (s0 + u) + 1] != 0.f)
+                     ? *reinterpret_cast<const float4*>(op + static_cast<size_t>(s0 + u) * kLatent)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
@@ -1058,7 +1097,7 @@ int decode_num_splits(int B, int H, int max_pages, int P, int num_sms) {
   // Long page tables get splits of at most ~kShareTiles tiles even past one wave: a ragged batch
   // then spreads its longest sequences over many CTAs while the shares of short sequences are
   // empty and exit at once, and the hardware backfills the SMs (split-major dispatch).
-  constexpr int kShareTiles = 80;
+  constexpr int kShareTiles = 40;
   const long long by_len = (max_sub + kShareTiles - 1) / kShareTiles;
   if (by_len > ns) ns = static_cast<int>(by_len > 64 ? 64 : by_len);
   int cap = static_cast<int>(max_sub / 4);
@@ -1085,6 +1124,16 @@ int decode_num_protected(int B, int H, int max_pages, int P, int S, int W, int n
   return static_cast<int>(nq < 1 ? 1 : (nq > prot_max ? prot_max : nq));
 }
 
+int decode_share_slots(int B, int H, int max_pages, int P, int n_split, int n_q, int num_sms) {
+  // balanced shares only when more shares are launched than one wave holds (long tables)
+  const int groups = B * (H / 16);
+  const int one_wave = kCtasPerSm * num_sms / (groups > 0 ? groups : 1) - 1;
+  if (decode_uses_tc(H) || n_split <= (one_wave > 1 ? one_wave : 1)) return 0;
+  const long long slots = static_cast<long long>(kCtasPerSm) * (num_sms > 0 ? num_sms : 1) -
+                          static_cast<long long>(groups) * n_q;
+  return static_cast<int>(slots > 16 ? (slots > (1 << 30) ? (1 << 30) : slots) : 16);
+}
+
 size_t decode_workspace_bytes(int B, int H, int n_slots) {
   const size_t NS = static_cast<size_t>(n_slots);
   return static_cast<size_t>(B) * H * NS * (kLatent + 2) * sizeof(float);
@@ -1092,7 +1141,7 @@ size_t decode_workspace_bytes(int B, int H, int n_slots) {
 
 // The dynamic shared-memory opt-in is a per-device function attribute: set it once per device
 // (never inside a stream capture after the first call).
-template <int BITS>
+template <int BITS, bool kBalanced>
 cudaError_t ensure_smem_attr() {
   static bool done[64] = {};
   int dev = 0;
@@ -1100,7 +1149,8 @@ cudaError_t ensure_smem_attr() {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!done[dev]) {
-    e = cudaFuncSetAttribute(decode_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<BITS>());
+    e = cudaFuncSetAttribute(decode_kernel<BITS, kBalanced>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<BITS>());
     if (e != cudaSuccess) return e;
     done[dev] = true;
   }
@@ -1112,12 +1162,23 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   const bool tc = decode_uses_tc(p.H);
   const dim3 grid(p.B, p.H / 16, tc ? p.n_q : p.n_q + p.n_split);
   cudaError_t e;
+  const bool bal = !tc && p.share_slots > 0;
   if (p.bits_c == 4) {
-    if ((e = ensure_smem_attr<4>()) != cudaSuccess) return e;
-    decode_kernel<4><<<grid, kThreads, smem_bytes<4>(), stream>>>(p);
+    if (bal) {
+      if ((e = ensure_smem_attr<4, true>()) != cudaSuccess) return e;
+      decode_kernel<4, true><<<grid, kThreads, smem_bytes<4>(), stream>>>(p);
+    } else {
+      if ((e = ensure_smem_attr<4, false>()) != cudaSuccess) return e;
+      decode_kernel<4, false><<<grid, kThreads, smem_bytes<4>(), stream>>>(p);
+    }
   } else {
-    if ((e = ensure_smem_attr<2>()) != cudaSuccess) return e;
-    decode_kernel<2><<<grid, kThreads, smem_bytes<2>(), stream>>>(p);
+    if (bal) {
+      if ((e = ensure_smem_attr<2, true>()) != cudaSuccess) return e;
+      decode_kernel<2, true><<<grid, kThreads, smem_bytes<2>(), stream>>>(p);
+    } else {
+      if ((e = ensure_smem_attr<2, false>()) != cudaSuccess) return e;
+      decode_kernel<2, false><<<grid, kThreads, smem_bytes<2>(), stream>>>(p);
+    }
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -64,6 +64,8 @@ struct DecodeParams {
   int p_shift;  // log2(P): page sizes are powers of two
   int n_split;  // shares of the packed tokens (partial slots 0 .. n_split-1)
   int n_q;      // CTAs sharing the protected (BF16) tokens (partial slots n_split .. n_split+n_q-1)
+  int share_slots;  // resident CTA slots of one wave left for packed shares (16-head kernel);
+                    // > 0: balanced equal shares (more shares launched than one wave holds)
 };
 
 // Number of packed-token shares, and of CTAs for the protected tokens, of each (sequence,
@@ -71,6 +73,7 @@ struct DecodeParams {
 int decode_num_splits(int B, int H, int max_pages, int P, int num_sms);
 int decode_num_protected(int B, int H, int max_pages, int P, int S, int W, int num_sms);
 size_t decode_workspace_bytes(int B, int H, int n_slots);  // n_slots = n_split + n_q
+int decode_share_slots(int B, int H, int max_pages, int P, int n_split, int n_q, int num_sms);
 // Head counts that are multiples of 64 run the packed shares on tcgen05 tensor cores (64 heads
 // per CTA, one CTA per SM); the others on the 16-head warp-level kernel.
 inline bool decode_uses_tc(int H) { return H % 64 == 0; }

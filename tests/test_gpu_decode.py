@@ -161,3 +161,15 @@ def test_tc_bad_page_sets_error_bit():
     torch.cuda.synchronize()
     assert cache.error_bits() & 1
     assert torch.isfinite(out).all()
+
+
+def test_balanced_shares_few_long_many_short():
+    """A wide page table with many sequences launches more shares than one wave holds, so the
+    16-head kernel takes equal shares sized from the batch: three long sequences among 61 short
+    and empty ones (shares past a sequence's end are empty)."""
+    w = workloads.WORKLOADS["ragged_c2r4_b64_h16_serve"]
+    rng = np.random.default_rng(17)
+    lens = rng.integers(0, 2000, size=64)
+    lens[[3, 40, 63]] = [12000, 11000, 9000]
+    lens[::9] = 0
+    _run(w, lens)
