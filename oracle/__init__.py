@@ -97,6 +97,10 @@ def lib():
         _lib.oracle_decode.argtypes = [P(Config), ctypes.c_int, ctypes.c_int, P(u16), P(u16), P(i32),
                                        ctypes.c_int, P(i32), P(u8), ctypes.c_int64, P(u16), P(u16),
                                        ctypes.c_float, P(d), P(d)]
+        _lib.oracle_decode_bf16.restype = ctypes.c_int
+        _lib.oracle_decode_bf16.argtypes = [ctypes.c_int, ctypes.c_int, P(u16), P(u16), P(i32), ctypes.c_int,
+                                            ctypes.c_int, P(i32), P(u16), ctypes.c_int64, ctypes.c_float, P(d),
+                                            P(d)]
     return _lib
 
 
@@ -220,4 +224,23 @@ def decode(cfg: Config, q_lat, q_rope, page_table, seq_lens, pool, sink, ring, s
                              _ptr(pool, ctypes.c_uint8), pool.shape[0], _ptr(sink_arg, ctypes.c_uint16),
                              _ptr(ring, ctypes.c_uint16), ctypes.c_float(softmax_scale),
                              _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    return out, lse, int(fl)
+
+
+def decode_bf16(q_lat, q_rope, page_table, page_size: int, seq_lens, kv_pool, softmax_scale: float):
+    """Exact attention over a paged BF16 cache kv_pool uint16[n_pages, P, 576] (the
+    unquantized comparator). Returns (out float64[B,H,512], lse float64[B,H], flags)."""
+    q_lat = np.ascontiguousarray(q_lat, dtype=np.uint16)
+    q_rope = np.ascontiguousarray(q_rope, dtype=np.uint16)
+    page_table = np.ascontiguousarray(page_table, dtype=np.int32)
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    kv_pool = np.ascontiguousarray(kv_pool, dtype=np.uint16)
+    B, H = q_lat.shape[0], q_lat.shape[1]
+    out = np.zeros((B, H, LATENT), dtype=np.float64)
+    lse = np.zeros((B, H), dtype=np.float64)
+    fl = lib().oracle_decode_bf16(B, H, _ptr(q_lat, ctypes.c_uint16), _ptr(q_rope, ctypes.c_uint16),
+                                  _ptr(page_table, ctypes.c_int32), page_table.shape[1], int(page_size),
+                                  _ptr(seq_lens, ctypes.c_int32), _ptr(kv_pool, ctypes.c_uint16),
+                                  kv_pool.shape[0], ctypes.c_float(softmax_scale), _ptr(out, ctypes.c_double),
+                                  _ptr(lse, ctypes.c_double))
     return out, lse, int(fl)

@@ -450,6 +450,48 @@ int oracle_token_values(const oracle_config* cfg, int b, int t, int T, const int
  *   out = sum_t exp(s_t - m) v_t[0:512] / l,  lse = m + ln l
  * T = 0 gives out = 0 and lse = -inf. Returns ERR_* flags (bad pages are skipped).
  */
+/* Exact attention of one sequence over its gathered token rows V[T][576] (ok[t] = row usable):
+ * scores s_t = scale * (q . v_t), one softmax over all usable tokens, O = sum_t p_t v_t[0:512],
+ * LSE natural log (QuantMLA page, appendix Figure 8: one global softmax, latent readout). */
+static void attend_rows(int H, const uint16_t* q_lat_b, const uint16_t* q_rope_b, const double* V,
+                        const char* ok, int T, float softmax_scale, double* out_b, double* lse_b) {
+#pragma omp parallel for schedule(dynamic)
+  for (int h = 0; h < H; ++h) {
+    double q[ROW];
+    for (int k = 0; k < LATENT; ++k) q[k] = oracle_bf16_to_double(q_lat_b[(size_t)h * LATENT + k]);
+    for (int j = 0; j < ROPE; ++j) q[LATENT + j] = oracle_bf16_to_double(q_rope_b[(size_t)h * ROPE + j]);
+    double* o = out_b + (size_t)h * LATENT;
+    for (int k = 0; k < LATENT; ++k) o[k] = 0.0;
+    double* s = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    double m = -INFINITY;
+    int any = 0;
+    for (int t = 0; t < T; ++t) {
+      if (!ok[t]) continue;
+      const double* v = V + (size_t)t * ROW;
+      double dot = 0.0;
+      for (int k = 0; k < ROW; ++k) dot += q[k] * v[k];
+      s[t] = (double)softmax_scale * dot;
+      if (!any || s[t] > m) m = s[t];
+      any = 1;
+    }
+    if (!any) {
+      lse_b[h] = -INFINITY;
+    } else {
+      double l = 0.0;
+      for (int t = 0; t < T; ++t) {
+        if (!ok[t]) continue;
+        double w = exp(s[t] - m);
+        l += w;
+        const double* v = V + (size_t)t * ROW;
+        for (int k = 0; k < LATENT; ++k) o[k] += w * v[k];
+      }
+      for (int k = 0; k < LATENT; ++k) o[k] /= l;
+      lse_b[h] = m + log(l);
+    }
+    free(s);
+  }
+}
+
 int oracle_decode(const oracle_config* cfg, int B, int H, const uint16_t* q_lat,
                   const uint16_t* q_rope, const int32_t* page_table, int max_pages,
                   const int32_t* seq_lens, const uint8_t* pool, int64_t n_pages,
@@ -470,41 +512,41 @@ int oracle_decode(const oracle_config* cfg, int B, int H, const uint16_t* q_lat,
       ok[t] = r >= 0;
       if (r < 0) flags |= ERR_BAD_PAGE;
     }
-#pragma omp parallel for schedule(dynamic)
-    for (int h = 0; h < H; ++h) {
-      double q[ROW];
-      for (int k = 0; k < LATENT; ++k) q[k] = oracle_bf16_to_double(q_lat[((size_t)b * H + h) * LATENT + k]);
-      for (int j = 0; j < ROPE; ++j) q[LATENT + j] = oracle_bf16_to_double(q_rope[((size_t)b * H + h) * ROPE + j]);
-      double* o = out + ((size_t)b * H + h) * LATENT;
-      for (int k = 0; k < LATENT; ++k) o[k] = 0.0;
-      double* s = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
-      double m = -INFINITY;
-      int any = 0;
-      for (int t = 0; t < T; ++t) {
-        if (!ok[t]) continue;
-        const double* v = V + (size_t)t * ROW;
-        double dot = 0.0;
-        for (int k = 0; k < ROW; ++k) dot += q[k] * v[k];
-        s[t] = (double)softmax_scale * dot;
-        if (!any || s[t] > m) m = s[t];
-        any = 1;
-      }
-      if (!any) {
-        lse[(size_t)b * H + h] = -INFINITY;
-      } else {
-        double l = 0.0;
-        for (int t = 0; t < T; ++t) {
-          if (!ok[t]) continue;
-          double w = exp(s[t] - m);
-          l += w;
-          const double* v = V + (size_t)t * ROW;
-          for (int k = 0; k < LATENT; ++k) o[k] += w * v[k];
-        }
-        for (int k = 0; k < LATENT; ++k) o[k] /= l;
-        lse[(size_t)b * H + h] = m + log(l);
-      }
-      free(s);
+    attend_rows(H, q_lat + (size_t)b * H * LATENT, q_rope + (size_t)b * H * ROPE, V, ok, T, softmax_scale,
+                out + (size_t)b * H * LATENT, lse + (size_t)b * H);
+    free(V);
+    free(ok);
+  }
+  return flags;
+}
+
+/* The unquantized comparator: the same attention over a paged BF16 cache, token t of sequence
+ * b in row t % P of page page_table[b][t / P] of kv_pool [n_pages][P][576] (c then k_R). */
+int oracle_decode_bf16(int B, int H, const uint16_t* q_lat, const uint16_t* q_rope,
+                       const int32_t* page_table, int max_pages, int page_size, const int32_t* seq_lens,
+                       const uint16_t* kv_pool, int64_t n_pages, float softmax_scale, double* out,
+                       double* lse) {
+  int flags = 0;
+  for (int b = 0; b < B; ++b) {
+    int T = seq_lens[b];
+    if (T < 0 || (int64_t)T > (int64_t)max_pages * page_size) {
+      flags |= ERR_SEQ_OVERFLOW;
+      T = 0;
     }
+    double* V = (double*)malloc(sizeof(double) * ((size_t)(T > 0 ? T : 1)) * ROW);
+    char* ok = (char*)malloc((size_t)(T > 0 ? T : 1));
+    for (int t = 0; t < T; ++t) {
+      const int32_t pid = page_table[(size_t)b * max_pages + t / page_size];
+      ok[t] = pid >= 0 && pid < n_pages;
+      if (!ok[t]) {
+        flags |= ERR_BAD_PAGE;
+        continue;
+      }
+      const uint16_t* row = kv_pool + ((size_t)pid * page_size + (size_t)(t % page_size)) * ROW;
+      for (int k = 0; k < ROW; ++k) V[(size_t)t * ROW + k] = oracle_bf16_to_double(row[k]);
+    }
+    attend_rows(H, q_lat + (size_t)b * H * LATENT, q_rope + (size_t)b * H * ROPE, V, ok, T, softmax_scale,
+                out + (size_t)b * H * LATENT, lse + (size_t)b * H);
     free(V);
     free(ok);
   }
