@@ -49,6 +49,11 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="latency sweep: C4R4 decode against the BF16 paged comparator over 1K..1M tokens")
+    ap.add_argument("--sweep-batches", default="1,8,32")
+    ap.add_argument("--sweep-heads", type=int, default=16)
+    ap.add_argument("--sweep-max-tokens", type=int, default=1 << 20)
     return ap.parse_args()
 
 
@@ -493,6 +498,136 @@ def e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream):
                     "layer as CUDA graphs, layer caches rotated as in the timed steps"}
 
 
+# ------------------------------------------------------------------ latency sweep against BF16
+
+SWEEP_BATCH_TOKENS = 1 << 23  # largest batch x context swept (bounds device memory and build time)
+FLUSH_BYTES = 512 * 1024 * 1024
+
+
+def bf16_decode_bytes(seq_lens, heads) -> int:
+    """Bytes the unquantized decode must move: every token's BF16 row, queries and outputs."""
+    B = len(seq_lens)
+    return int(sum(int(T) for T in seq_lens)) * 576 * 2 + B * heads * 576 * 2 + B * heads * (512 + 1) * 4
+
+
+def run_sweep(args):
+    """Decode latency of one layer over a C4R4 cache (page 128, sink 4, recent 128) and over an
+    unquantized BF16 paged cache (page 64) holding the same tokens, for contexts of 1K..1M tokens
+    and batches 1/8/32, as the normalised-latency tables of the low-bit MLA cache pages report:
+    delta = t_C4R4 / t_BF16 - 1. Both calls are captured as CUDA graphs; a 512 MB write before
+    every timed call evicts L2, so each call reads its cache from HBM (one decode of one layer,
+    whose cache the other layers' calls have evicted). Every sequence of a batch holds the same
+    synthetic rows (one seeded 1M-token draw; prefixes give the shorter contexts)."""
+    import torch
+
+    import bit_mla_kv_qcache_gb300 as q
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    H = args.sweep_heads
+    t_max = args.sweep_max_tokens
+    batches = [int(x) for x in args.sweep_batches.split(",") if x]
+    contexts = [1024 << i for i in range(11) if (1024 << i) <= t_max]
+    wq = workloads.Workload("sweep_c4r4", 1, H, max(contexts), 4, 128)
+    inp = workloads.make_inputs(wq, extra_pages=0)
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else
+                                        np.ascontiguousarray(a)).to(dev)
+    c_all, kr_all = to_dev(inp.c), to_dev(inp.kr)
+    q1_lat, q1_rope = to_dev(inp.q_lat), to_dev(inp.q_rope)  # [1, H, *]: one query row, every sequence
+    cfg = q.make_config(**wq.config_kwargs())
+    P_q, P_b = wq.page_size, 64
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    hbm_peak, _, peak_kind = peaks()
+    rng = np.random.default_rng(77)
+    iters = max(10, args.steps)
+    points = []
+    with ClockSampler(0) as clk:
+        for B in batches:
+            q_lat, q_rope = q1_lat.expand(B, H, 512).contiguous(), q1_rope.expand(B, H, 64).contiguous()
+            out = torch.empty((B, H, 512), dtype=torch.float32, device=dev)
+            lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+            for T in contexts:
+                if B * T > SWEEP_BATCH_TOKENS:
+                    continue
+                lens = torch.full((B,), T, dtype=torch.int32, device=dev)
+                # C4R4 cache: sequence by sequence through the writer (rows of one sequence only)
+                mp_q = math.ceil(T / P_q) + 1
+                pt_q, np_q = workloads.page_table_for(rng, B, mp_q, True)
+                cache = q.QuantizedMLACache(cfg, B, mp_q, np_q, page_table=to_dev(pt_q), device=dev)
+                cu = torch.zeros(B + 1, dtype=torch.int32, device=dev)
+                for b in range(B):
+                    cu.zero_()
+                    cu[b + 1:] = T
+                    cache.write(c_all[:T], kr_all[:T], cu, T)
+                # BF16 paged cache: the same rows, scattered into 64-token pages
+                mp_b = math.ceil(T / P_b) + 1
+                pt_b, np_b = workloads.page_table_for(rng, B, mp_b, True)
+                d_pt_b = to_dev(pt_b)
+                pool = torch.zeros((np_b, P_b, 576), dtype=torch.int16, device=dev)
+                rows = torch.cat([c_all[:T], kr_all[:T]], dim=1)
+                tok = torch.arange(T, device=dev, dtype=torch.int64)
+                for b in range(B):
+                    slot = d_pt_b[b].to(torch.int64)[tok // P_b] * P_b + tok % P_b
+                    pool.view(-1, 576)[slot] = rows
+                del rows, tok
+                err = torch.zeros(1, dtype=torch.int32, device=dev)
+                ws_q = cache.workspace(H)
+                ws_b = torch.empty(q.bf16_workspace_bytes(B, H, mp_b, P_b), dtype=torch.uint8, device=dev)
+                torch.cuda.synchronize()
+                if cache.error_bits():
+                    raise RuntimeError("writer reported device errors while building the sweep cache")
+
+                def call_q():
+                    q.mla_qcache_decode_attn(cfg, q_lat, q_rope, cache.page_table, lens, cache.pool, cache.sink,
+                                             cache.ring, wq.softmax_scale, out, lse, ws_q, cache.err)
+
+                def call_b():
+                    q.mla_qcache_decode_attn_bf16(q_lat, q_rope, d_pt_b, P_b, lens, pool, wq.softmax_scale, out, lse,
+                                                  ws_b, err)
+
+                graphs = []
+                with torch.cuda.stream(stream):
+                    for fn in (call_q, call_b):
+                        fn()
+                        torch.cuda.synchronize()
+                        g = torch.cuda.CUDAGraph()
+                        with torch.cuda.graph(g, stream=stream):
+                            fn()
+                        graphs.append(g)
+                    times = [[], []]
+                    for k in range(3 + iters):  # both sides alternate under the same clocks
+                        for side in (0, 1):
+                            flush.fill_(float(k))
+                            s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                            s_ev.record(stream)
+                            graphs[side].replay()
+                            e_ev.record(stream)
+                            if k >= 3:
+                                times[side].append((s_ev, e_ev))
+                    torch.cuda.synchronize()
+                if cache.error_bits() or int(err.item()):
+                    raise RuntimeError("device error bits set during the sweep")
+                us = [statistics.median(a.elapsed_time(b) * 1e3 for a, b in ts) for ts in times]
+                seq = [T] * B
+                wb = workloads.Workload("sweep_c4r4", B, H, T, 4, 128)
+                bq, bb = decode_bytes(wb, seq, H), bf16_decode_bytes(seq, H)
+                points.append({"batch": B, "T": T, "c4r4_us": us[0], "bf16_us": us[1], "delta": us[0] / us[1] - 1.0,
+                               "c4r4_hbm_frac": bq / (us[0] * 1e-6) / 1e9 / hbm_peak,
+                               "bf16_hbm_frac": bb / (us[1] * 1e-6) / 1e9 / hbm_peak,
+                               "c4r4_bytes": bq, "bf16_bytes": bb})
+                del graphs, cache, pool, ws_q, ws_b
+                torch.cuda.empty_cache()
+    print(json.dumps({
+        "mode": "latency_sweep", "metric": "decode attention latency per layer, C4R4 vs BF16 paged; "
+                                           "delta = t_C4R4 / t_BF16 - 1", "unit": "us", "heads": H,
+        "cache": "C4R4 page 128 sink 4 recent 128", "comparator": "BF16 paged cache, page 64 (own kernel)",
+        "iters": iters, "statistic": "median", "l2": "512 MB write before every timed call",
+        "hbm_peak_gbs": hbm_peak, "peak_kind": peak_kind, "data": "synthetic", "points": points,
+        "clocks": clk.summary()}))
+    return 0
+
+
 def cpu_baseline(w):
     n_seq = max(1, w.batch // 16)
     step, scale = oracle_step_sample(w, n_seq)
@@ -509,6 +644,8 @@ def main():
     w = workloads.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.sweep:
+        return run_sweep(args)
     return run_native(args, w)
 
 

@@ -5,10 +5,12 @@ The compute path is the CUDA library libmla_qcache.so (C ABI in include/mla_qcac
 buffers (pool, BF16 sink/recent buffers, workspace) of one layer.
 """
 from .binding import (DEV_BAD_PAGE, DEV_NONFINITE, DEV_RANGE, DEV_ROWS, DEV_SEQ_OVERFLOW, DEV_TIMEOUT, EXPORTS,
-                      Config, QCacheError, lib, make_config, mla_qcache_advance, mla_qcache_decode_attn,
+                      Config, QCacheError, bf16_workspace_bytes, lib, make_config, mla_qcache_advance,
+                      mla_qcache_decode_attn, mla_qcache_decode_attn_bf16,
                       mla_qcache_write, mla_qcache_write_advance, page_bytes, strerror, workspace_bytes)
 from .cache import QuantizedMLACache
 
 __all__ = ["Config", "QCacheError", "QuantizedMLACache", "lib", "make_config", "mla_qcache_advance", "mla_qcache_decode_attn",
-           "mla_qcache_write", "mla_qcache_write_advance", "page_bytes", "strerror", "workspace_bytes", "EXPORTS", "DEV_BAD_PAGE",
+           "mla_qcache_write", "mla_qcache_write_advance", "mla_qcache_decode_attn_bf16", "bf16_workspace_bytes",
+           "page_bytes", "strerror", "workspace_bytes", "EXPORTS", "DEV_BAD_PAGE",
            "DEV_NONFINITE", "DEV_RANGE", "DEV_ROWS", "DEV_SEQ_OVERFLOW", "DEV_TIMEOUT"]

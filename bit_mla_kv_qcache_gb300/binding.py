@@ -21,7 +21,7 @@ DEV_BAD_PAGE, DEV_SEQ_OVERFLOW, DEV_NONFINITE, DEV_RANGE, DEV_ROWS, DEV_TIMEOUT 
 EXPORTS = ("mla_qcache_page_bytes", "mla_qcache_config_check", "mla_qcache_workspace_bytes",
            "mla_qcache_write", "mla_qcache_decode_attn", "mla_qcache_strerror",
            "mla_qcache_decode_attn_noalloc", "mla_qcache_noalloc_scratch_bytes", "mla_qcache_advance",
-           "mla_qcache_write_advance")
+           "mla_qcache_write_advance", "mla_qcache_decode_attn_bf16", "mla_qcache_bf16_workspace_bytes")
 
 
 class Config(ctypes.Structure):
@@ -75,6 +75,11 @@ def lib() -> ctypes.CDLL:
         L.mla_qcache_write_advance.restype = ctypes.c_int
         L.mla_qcache_write_advance.argtypes = [P(Config), i32, i32, vp, vp, vp, vp, vp, i32, vp, i32, vp, i64, vp, vp,
                                                vp, vp]
+        L.mla_qcache_bf16_workspace_bytes.restype = sz
+        L.mla_qcache_bf16_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        L.mla_qcache_decode_attn_bf16.restype = ctypes.c_int
+        L.mla_qcache_decode_attn_bf16.argtypes = [i32, i32, vp, vp, vp, i32, i32, vp, vp, i64, ctypes.c_float, vp, vp,
+                                                  vp, sz, vp, vp]
         L.mla_qcache_advance.restype = ctypes.c_int
         L.mla_qcache_advance.argtypes = [vp, vp, i32, vp]
         L.mla_qcache_strerror.restype = ctypes.c_char_p
@@ -150,6 +155,26 @@ def mla_qcache_write_advance(cfg: Config, c_new, kr_new, cu_new, seq_lens, seq_l
         pool.shape[0], _ptr(sink_buf, "sink_buf", 2, allow_none=True) if cfg.n_sink else None,
         _ptr(recent_buf, "recent_buf", 2), _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
     _raise(st, "mla_qcache_write_advance")
+
+
+def bf16_workspace_bytes(B: int, H: int, max_pages: int, page_size: int) -> int:
+    return int(lib().mla_qcache_bf16_workspace_bytes(B, H, max_pages, page_size))
+
+
+def mla_qcache_decode_attn_bf16(q_lat, q_rope, page_table, page_size: int, seq_lens, kv_pool, softmax_scale: float,
+                                out, lse, workspace, err_word, stream=None) -> None:
+    """Decode attention over a paged BF16 cache kv_pool [n_pages, page_size, 576] (the
+    unquantized comparator, see include/mla_qcache.h)."""
+    B, H = q_lat.shape[0], q_lat.shape[1]
+    if kv_pool.dim() != 3 or kv_pool.shape[1] != page_size or kv_pool.shape[2] != 576:
+        raise ValueError(f"kv_pool must be [n_pages, {page_size}, 576], got {tuple(kv_pool.shape)}")
+    st = lib().mla_qcache_decode_attn_bf16(
+        B, H, _ptr(q_lat, "q_lat", 2), _ptr(q_rope, "q_rope", 2), _ptr(page_table, "page_table", dtype=torch.int32),
+        page_table.shape[1], int(page_size), _ptr(seq_lens, "seq_lens", dtype=torch.int32),
+        _ptr(kv_pool, "kv_pool", 2), kv_pool.shape[0], ctypes.c_float(softmax_scale),
+        _ptr(out, "out", dtype=torch.float32), _ptr(lse, "lse", dtype=torch.float32), _ptr(workspace, "workspace", 1),
+        workspace.numel(), _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
+    _raise(st, "mla_qcache_decode_attn_bf16")
 
 
 def mla_qcache_advance(cu_new, seq_lens, stream=None) -> None:

@@ -225,6 +225,59 @@ int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H, c
   return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
 }
 
+size_t mla_qcache_bf16_workspace_bytes(int32_t B, int32_t H, int32_t max_pages, int32_t page_size) {
+  if (B < 1 || H < 16 || H > 256 || H % 16 || max_pages < 1 ||
+      (page_size != 32 && page_size != 64 && page_size != 128))
+    return 0;
+  int sms = 0;
+  if (current_sm_count(&sms) != MLA_QCACHE_OK) return 0;
+  return mlaq::decode_workspace_bytes(B, H, mlaq::decode_bf16_num_parts(B, H, max_pages, page_size, sms));
+}
+
+int mla_qcache_decode_attn_bf16(int32_t B, int32_t H, const uint16_t* q_lat, const uint16_t* q_rope,
+                                const int32_t* page_table, int32_t max_pages, int32_t page_size,
+                                const int32_t* seq_lens, const uint16_t* kv_pool, int64_t n_pages,
+                                float softmax_scale, float* out, float* lse, void* workspace,
+                                size_t workspace_bytes, int32_t* err_word, void* stream) {
+  if (B < 1 || B > (1 << 20) || H < 16 || H > 256 || H % 16 || max_pages < 1 || n_pages < 1)
+    return MLA_QCACHE_ERR_SHAPE;
+  if (page_size != 32 && page_size != 64 && page_size != 128) return MLA_QCACHE_ERR_CONFIG;
+  if (!q_lat || !q_rope || !page_table || !seq_lens || !kv_pool || !out || !lse || !workspace || !err_word)
+    return MLA_QCACHE_ERR_NULL;
+  if (!aligned(q_lat, 4) || !aligned(q_rope, 4) || !aligned(kv_pool, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+      !aligned(workspace, 16) || !aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(err_word, 4))
+    return MLA_QCACHE_ERR_ALIGN;
+  int sms = 0;
+  int st = current_sm_count(&sms);
+  if (st != MLA_QCACHE_OK) return st;
+  const int parts = mlaq::decode_bf16_num_parts(B, H, max_pages, page_size, sms);
+  if (workspace_bytes < mlaq::decode_workspace_bytes(B, H, parts)) return MLA_QCACHE_ERR_WORKSPACE;
+  mlaq::DecodeParams p{};
+  p.q_lat = q_lat;
+  p.q_rope = q_rope;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.kv_bf16 = kv_pool;
+  p.o_part = static_cast<float*>(workspace);
+  p.ml_part = static_cast<float*>(workspace) + static_cast<size_t>(B) * H * parts * mlaq::kLatent;
+  p.out = out;
+  p.lse = lse;
+  p.err = err_word;
+  p.n_pages = n_pages;
+  p.scale_log2 = static_cast<float>(static_cast<double>(softmax_scale) * 1.4426950408889634074);
+  p.B = B;
+  p.H = H;
+  p.max_pages = max_pages;
+  p.P = page_size;
+  p.p_shift = 0;
+  while ((1 << p.p_shift) < p.P) ++p.p_shift;
+  p.bits_c = 4;
+  p.n_split = 0;  // every share is a BF16 share
+  p.n_q = parts;
+  const cudaError_t e = mlaq::launch_decode_bf16(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
+}
+
 int mla_qcache_decode_attn_noalloc(const mla_qcache_config* cfg, int32_t B, int32_t H, const uint16_t* q_lat,
                                    const uint16_t* q_rope, const int32_t* page_table, int32_t max_pages,
                                    const int32_t* seq_lens, const uint8_t* pool, int64_t n_pages,

@@ -238,18 +238,36 @@ __device__ __forceinline__ void load_p(const Shared& sh, int buf, float2 (&pf)[4
 }
 
 // ------------------------------------------------------------------ protected (BF16) tokens
+// kPaged: every token of the sequence from a paged BF16 cache (the unquantized comparator);
+// else the sink and recent tokens from the BF16 retention buffers.
+template <bool kPaged>
 __device__ void bf16_split(const DecodeParams& p, const Shared& sh, int b, int T, int part,
                            const uint32_t (&qa)[8][4], const uint32_t (&qra)[4], State& st, int32_t& flags) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int s_end = min(p.S, T);
-  const int r_beg = max(T - p.W, s_end);
+  const int s_end = kPaged ? 0 : min(p.S, T);
+  const int r_beg = kPaged ? 0 : max(T - p.W, s_end);
   const int has_sink = s_end > 0 ? 1 : 0;
   const int n_all = has_sink + (T - r_beg + kTile - 1) / kTile;
   // this CTA's share of the sequence's protected tiles: [t_lo, t_lo + n_tiles)
-  const int t_lo = (n_all * part) / p.n_q;
-  const int n_tiles = (n_all * (part + 1)) / p.n_q - t_lo;
+  // (64-bit products only for the paged comparator, whose tables reach millions of tokens)
+  const int t_lo = kPaged ? static_cast<int>((static_cast<long long>(n_all) * part) / p.n_q) : (n_all * part) / p.n_q;
+  const int n_tiles =
+      (kPaged ? static_cast<int>((static_cast<long long>(n_all) * (part + 1)) / p.n_q) : (n_all * (part + 1)) / p.n_q) -
+      t_lo;
   if (n_tiles <= 0) return;
   constexpr int kStageBytes = kTile * kBf16RowBytes;
+  if constexpr (kPaged) {  // validate the share's page ids before any copy reads through them
+    bool bad = false;
+    const int pg_lo = (t_lo * kTile) >> p.p_shift, pg_hi = (min(T, (t_lo + n_tiles) * kTile) - 1) >> p.p_shift;
+    for (int pg = pg_lo + static_cast<int>(threadIdx.x); pg <= pg_hi; pg += kThreads) {
+      const int32_t pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
+      bad |= pid < 0 || pid >= p.n_pages;
+    }
+    if (__syncthreads_or(bad)) {
+      flags |= kErrBadPage;
+      return;
+    }
+  }
 
   auto tile_range = [&](int li, int& start, int& count) {  // li: index in this CTA's share
     const int i = t_lo + li;
@@ -262,8 +280,13 @@ __device__ void bf16_split(const DecodeParams& p, const Shared& sh, int b, int T
     }
   };
   auto row_ptr = [&](int t) -> const uint16_t* {
-    return t < p.S ? p.sink + (static_cast<size_t>(b) * p.S + t) * kRow
-                   : p.ring + (static_cast<size_t>(b) * p.W + (t % p.W)) * kRow;
+    if constexpr (kPaged) {
+      const int32_t pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + (t >> p.p_shift));
+      return p.kv_bf16 + (static_cast<size_t>(pid) * p.P + (t & (p.P - 1))) * kRow;
+    } else {
+      return t < p.S ? p.sink + (static_cast<size_t>(b) * p.S + t) * kRow
+                     : p.ring + (static_cast<size_t>(b) * p.W + (t % p.W)) * kRow;
+    }
   };
   auto issue = [&](int i) {
     int start, count;
@@ -931,6 +954,7 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
 }
 
 // ------------------------------------------------------------------ protected-token CTA
+template <bool kPaged>
 __device__ void protected_split(const DecodeParams& p, const Shared& sh, int b, int T, int part, State& st,
                                 int32_t& flags) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
@@ -958,7 +982,7 @@ __device__ void protected_split(const DecodeParams& p, const Shared& sh, int b, 
     qra[2] = __ldg(r0 + 4 + q);
     qra[3] = __ldg(r1 + 4 + q);
   }
-  bf16_split(p, sh, b, T, part, qa, qra, st, flags);
+  bf16_split<kPaged>(p, sh, b, T, part, qa, qra, st, flags);
 
   const int NS = p.n_split + p.n_q, slot = p.n_split + part;
   float* o0 = p.o_part + ((static_cast<size_t>(b) * p.H + h0 + g) * NS + slot) * kLatent + 128 * warp;
@@ -972,7 +996,7 @@ __device__ void protected_split(const DecodeParams& p, const Shared& sh, int b, 
 
 // kBalanced: equal shares sized from the whole batch (launched when more shares than one wave
 // are needed); a separate instance, so the one-wave kernel carries none of its code.
-template <int BITS, bool kBalanced>
+template <int BITS, bool kBalanced, bool kPaged = false>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const Shared sh = carve<BITS>(smem);
@@ -1011,7 +1035,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
   st.m_run = -INFINITY;
   st.l_part = 0.f;
 
-  if (is_bf16) protected_split(p, sh, b, T, split - p.n_split, st, flags);
+  if (is_bf16) protected_split<kPaged>(p, sh, b, T, split - p.n_split, st, flags);
   else packed_split<BITS, kBalanced>(p, sh, b, T, split, st, flags);
 
   const int NS = p.n_split + p.n_q;
@@ -1183,6 +1207,40 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (tc && (e = launch_decode_tc(p, stream)) != cudaSuccess) return e;
+  combine_kernel<<<p.B * p.H, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// The unquantized comparator: every share a BF16 share over the paged BF16 cache.
+int decode_bf16_num_parts(int B, int H, int max_pages, int P, int num_sms) {
+  const int groups = B * (H / 16);
+  int ns = kCtasPerSm * num_sms / (groups > 0 ? groups : 1);
+  const long long max_tiles = (static_cast<long long>(max_pages) * P + kTile - 1) / kTile;
+  // Few sequence-head groups already fill the GPU with one wave of shares; only where one wave
+  // leaves a share well above ~128 16-token tiles (many groups, long tables) are shares made
+  // smaller, at the price of several waves.
+  const long long by_len = (max_tiles + 127) / 128;
+  if (by_len > 2LL * ns) ns = static_cast<int>(by_len > 512 ? 512 : by_len);
+  if (ns > max_tiles) ns = static_cast<int>(max_tiles);
+  if (ns < 1) ns = 1;
+  return ns;
+}
+
+cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t stream) {
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!done[dev]) {
+    e = cudaFuncSetAttribute(decode_kernel<4, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<4>());
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  const dim3 grid(p.B, p.H / 16, p.n_q);
+  decode_kernel<4, false, true><<<grid, kThreads, smem_bytes<4>(), stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   combine_kernel<<<p.B * p.H, 128, 0, stream>>>(p);
   return cudaGetLastError();
 }

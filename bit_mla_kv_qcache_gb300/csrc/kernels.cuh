@@ -52,6 +52,7 @@ struct DecodeParams {
   const uint8_t* pool;
   const uint16_t* sink;
   const uint16_t* ring;
+  const uint16_t* kv_bf16;  // paged BF16 cache of the unquantized comparator (else nullptr)
   float* o_part;  // [B][H][NS][512] partial (unnormalized) outputs
   float* ml_part; // [B][H][NS][2] partial (max in log2 units, sum)
   float* out;     // [B][H][512]
@@ -80,6 +81,9 @@ inline bool decode_uses_tc(int H) { return H % 64 == 0; }
 int decode_tc_num_splits(int B, int H, int max_pages, int P, int num_sms);
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+// Unquantized comparator: decode over a paged BF16 cache [n_pages][P][576] (every share BF16).
+int decode_bf16_num_parts(int B, int H, int max_pages, int P, int num_sms);
+cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t stream);
 
 // Built-in decode scratch for callers that cannot allocate (mla_qcache_decode_attn_noalloc).
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;

@@ -188,6 +188,24 @@ int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows,
                      uint16_t* recent_buf, int32_t* err_word, void* stream);
 
 /*
+ * Unquantized comparator: the same single-token decode attention over a paged BF16 cache
+ * (every token exact; the latency the quantized cache is measured against, QuantMLA page,
+ * appendix Table 9 form: delta = t_quantized / t_BF16 - 1).
+ *   kv_pool    [n_pages][page_size][576] BF16 (c then k_R per token), 16-byte aligned; token
+ *              t of sequence b lives in row t % page_size of page page_table[b][t / page_size].
+ *   page_size  32, 64 or 128. Other arguments as mla_qcache_decode_attn (no sink/recent
+ *              buffers, no quantization config); workspace of mla_qcache_bf16_workspace_bytes.
+ * Errors: as mla_qcache_decode_attn; a bad page id sets MLA_QCACHE_DEV_BAD_PAGE and drops the
+ * share that would read it.
+ */
+size_t mla_qcache_bf16_workspace_bytes(int32_t B, int32_t H, int32_t max_pages, int32_t page_size);
+int mla_qcache_decode_attn_bf16(int32_t B, int32_t H, const uint16_t* q_lat, const uint16_t* q_rope,
+                                const int32_t* page_table, int32_t max_pages, int32_t page_size,
+                                const int32_t* seq_lens, const uint16_t* kv_pool, int64_t n_pages,
+                                float softmax_scale, float* out, float* lse, void* workspace,
+                                size_t workspace_bytes, int32_t* err_word, void* stream);
+
+/*
  * Fused cache writer with the length update: exactly mla_qcache_write, and in the same launch
  * seq_lens_next[b] = seq_lens[b] + cu_new[b+1] - cu_new[b] for every b in [0, B) (a decode
  * step then needs no separate length kernel). seq_lens_next [B] is a device int32 array,

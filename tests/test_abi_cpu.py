@@ -88,6 +88,15 @@ def test_host_validation_without_gpu(L):
     assert lib.mla_qcache_advance(p, None, 4, None) == -1
     assert lib.mla_qcache_advance(p, p, 0, None) == -3
     assert lib.mla_qcache_advance(ctypes.c_void_p(16 * 1024 + 2), p, 4, None) == -4
+    # unquantized comparator: shapes, page size, pointers, alignment
+    f = ctypes.c_float(0.1)
+    bf = lambda B, H, P, pool, ws: lib.mla_qcache_decode_attn_bf16(B, H, p, p, p, 4, P, p, pool, 8, f, p, p, ws, 1 << 20,
+                                                                   p, None)
+    assert bf(0, 16, 64, p, p) == -3 and bf(1, 24, 64, p, p) == -3
+    assert bf(1, 16, 48, p, p) == -2
+    assert bf(1, 16, 64, None, p) == -1
+    assert bf(1, 16, 64, ctypes.c_void_p(16 * 1024 + 4), p) == -4
+    assert lib.mla_qcache_bf16_workspace_bytes(1, 24, 4, 64) == 0 and lib.mla_qcache_bf16_workspace_bytes(1, 16, 4, 48) == 0
     # fused write + length update: a second, non-overlapping, aligned length array is required
     p2 = ctypes.c_void_p(32 * 1024)
     args = lambda lens, nxt: (ctypes.byref(cfg), 4, 4, p, p, p, lens, nxt, 1, p, 1, p, 1, p, p, p, None)
