@@ -612,7 +612,9 @@ def run_sweep(args):
                 seq = [T] * B
                 wb = workloads.Workload("sweep_c4r4", B, H, T, 4, 128)
                 bq, bb = decode_bytes(wb, seq, H), bf16_decode_bytes(seq, H)
+                bf16_floor_us = bb / (hbm_peak * 1e9) * 1e6  # the comparator at the measured copy bandwidth
                 points.append({"batch": B, "T": T, "c4r4_us": us[0], "bf16_us": us[1], "delta": us[0] / us[1] - 1.0,
+                               "bf16_roofline_us": bf16_floor_us, "delta_vs_bf16_roofline": us[0] / bf16_floor_us - 1.0,
                                "c4r4_hbm_frac": bq / (us[0] * 1e-6) / 1e9 / hbm_peak,
                                "bf16_hbm_frac": bb / (us[1] * 1e-6) / 1e9 / hbm_peak,
                                "c4r4_bytes": bq, "bf16_bytes": bb})

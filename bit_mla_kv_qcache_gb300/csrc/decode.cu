@@ -1110,6 +1110,82 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p) {
     p.lse[bh] = (m == -INFINITY || !(l > 0.f)) ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
 }
 
+// Many partials per (sequence, head), as a long table over few sequence-head groups gives: CTA
+// (bh, quarter) merges channels 128*quarter .. +127; its kWideGroups warps each take every
+// kWideGroups-th batch of partials, and the warps' sums are added in shared memory.
+constexpr int kWideGroups = 16;
+constexpr int kWideMinSlots = 33;  // fewer partials: combine_kernel
+__global__ void __launch_bounds__(32 * kWideGroups) combine_wide_kernel(const DecodeParams p) {
+  __shared__ float4 red[kWideGroups - 1][32];
+  const int bh = blockIdx.x, quarter = blockIdx.y;
+  const int NS = p.n_split + p.n_q;
+  const int grp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* ml = p.ml_part + static_cast<size_t>(bh) * NS * 2;
+  const float* op = p.o_part + static_cast<size_t>(bh) * NS * kLatent + 128 * quarter + 4 * lane;
+  // every warp forms the maximum and the weight sum over all partials (2 NS floats, cached)
+  float m = -INFINITY;
+  for (int s = lane; s < NS; s += 32) m = fmaxf(m, ml[2 * s]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float l = 0.f;
+  if (m != -INFINITY)
+    for (int s = lane; s < NS; s += 32) l += exp2f(ml[2 * s] - m) * ml[2 * s + 1];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (m != -INFINITY && l > 0.f) {
+    constexpr int kBatch = 8;
+    for (int s0 = grp * kBatch; s0 < NS; s0 += kWideGroups * kBatch) {
+      float w[kBatch];
+      float4 v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {  // a partial of weight zero (an empty share) is not read
+        w[u] = s0 + u < NS ? exp2f(ml[2 * (s0 + u)] - m) : 0.f;
+        v[u] = w[u] != 0.f ? *reinterpret_cast<const float4*>(op + static_cast<size_t>(s0 + u) * kLatent)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        acc.x += w[u] * v[u].x;
+        acc.y += w[u] * v[u].y;
+        acc.z += w[u] * v[u].z;
+        acc.w += w[u] * v[u].w;
+      }
+    }
+  }
+  if (grp > 0) red[grp - 1][lane] = acc;
+  __syncthreads();
+  if (grp != 0) return;
+  for (int g2 = 0; g2 < kWideGroups - 1; ++g2) {
+    const float4 r = red[g2][lane];
+    acc.x += r.x;
+    acc.y += r.y;
+    acc.z += r.z;
+    acc.w += r.w;
+  }
+  if (m != -INFINITY && l > 0.f) {
+    const float inv = 1.f / l;
+    acc.x *= inv;
+    acc.y *= inv;
+    acc.z *= inv;
+    acc.w *= inv;
+  }
+  *reinterpret_cast<float4*>(p.out + static_cast<size_t>(bh) * kLatent + 128 * quarter + 4 * lane) = acc;
+  if (quarter == 0 && lane == 0)
+    p.lse[bh] = (m == -INFINITY || !(l > 0.f)) ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
+}
+
+// The merge launch for a decode call: one CTA per (sequence, head), or four wide CTAs when the
+// partials are many.
+cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
+  if (p.n_split + p.n_q >= kWideMinSlots)
+    combine_wide_kernel<<<dim3(p.B * p.H, 4), 32 * kWideGroups, 0, stream>>>(p);
+  else
+    combine_kernel<<<p.B * p.H, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int decode_num_splits(int B, int H, int max_pages, int P, int num_sms) {
@@ -1123,11 +1199,11 @@ int decode_num_splits(int B, int H, int max_pages, int P, int num_sms) {
   // empty and exit at once, and the hardware backfills the SMs (split-major dispatch).
   constexpr int kShareTiles = 40;
   const long long by_len = (max_sub + kShareTiles - 1) / kShareTiles;
-  if (by_len > ns) ns = static_cast<int>(by_len > 64 ? 64 : by_len);
+  // (the rule only ever raises the count: a wave of shorter shares stays as it is)
+  if (by_len > ns && ns < 64) ns = static_cast<int>(by_len > 64 ? 64 : by_len);
   int cap = static_cast<int>(max_sub / 4);
   if (cap < 1) cap = 1;
   if (ns > cap) ns = cap;
-  if (ns > 64) ns = 64;
   if (ns < 1) ns = 1;
   return ns;
 }
@@ -1207,8 +1283,7 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (tc && (e = launch_decode_tc(p, stream)) != cudaSuccess) return e;
-  combine_kernel<<<p.B * p.H, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_combine(p, stream);
 }
 
 // The unquantized comparator: every share a BF16 share over the paged BF16 cache.
@@ -1241,8 +1316,7 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t stream) {
   const dim3 grid(p.B, p.H / 16, p.n_q);
   decode_kernel<4, false, true><<<grid, kThreads, smem_bytes<4>(), stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  combine_kernel<<<p.B * p.H, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_combine(p, stream);
 }
 
 // ------------------------------------------------------------------ built-in scratch

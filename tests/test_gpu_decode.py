@@ -173,3 +173,16 @@ def test_balanced_shares_few_long_many_short():
     lens[[3, 40, 63]] = [12000, 11000, 9000]
     lens[::9] = 0
     _run(w, lens)
+
+
+@pytest.mark.parametrize("T,bits", [(4000, 4), (5000, 4), (65536, 4), (40000, 2)])
+def test_one_sequence_many_splits(T, bits):
+    """One sequence over 16 heads spreads its packed tiles over up to a full wave of CTAs; past
+    32 partials per head the merge runs as four wide CTAs per (sequence, head)."""
+    _run(C4 if bits == 4 else C2, [T])
+
+
+def test_one_sequence_wide_table_full_wave():
+    """A page table far longer than the sequence (5000 tokens in a 5040-page table) still takes
+    one wave of shares, most of them empty."""
+    _run(C4, [5000], extra_pages=5000)
