@@ -11,8 +11,11 @@ may import this package. It shares no code with the CUDA library and never impor
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py`` against values
 that do not come from the oracle itself (numpy's float16, exact rational brute force, the
-effective-bits figures of Table 5, closed forms of softmax attention, and
-``torch.nn.functional.scaled_dot_product_attention`` in float64).
+effective-bits figures of Table 5, closed forms of softmax attention,
+``torch.nn.functional.scaled_dot_product_attention`` in float64, and for the cached-tensor
+transform: identity and signed-permutation closed forms, a hand-worked float32 sum that fixes
+the accumulation order, torch's float64 matmul within the float32 summation bound, and torch's
+BF16 rounding).
 """
 from __future__ import annotations
 
@@ -101,6 +104,9 @@ def lib():
         _lib.oracle_decode_bf16.argtypes = [ctypes.c_int, ctypes.c_int, P(u16), P(u16), P(i32), ctypes.c_int,
                                             ctypes.c_int, P(i32), P(u16), ctypes.c_int64, ctypes.c_float, P(d),
                                             P(d)]
+        _lib.oracle_row_transform.restype = None
+        _lib.oracle_row_transform.argtypes = [ctypes.c_int, ctypes.c_int, P(u16), P(u16), P(ctypes.c_float),
+                                              P(u16)]
     return _lib
 
 
@@ -244,3 +250,29 @@ def decode_bf16(q_lat, q_rope, page_table, page_size: int, seq_lens, kv_pool, so
                                   kv_pool.shape[0], ctypes.c_float(softmax_scale), _ptr(out, ctypes.c_double),
                                   _ptr(lse, ctypes.c_double))
     return out, lse, int(fl)
+
+
+# ------------------------------------------------------------------ cached-tensor transforms
+
+def row_transform(x_bits, a_bits):
+    """x A for BF16 rows x [n, d] and a BF16 matrix A [d, d] (RAQ-MLA page, Figure 4: A_c on the
+    latent, A_R on the positional key before caching). Float32 sums in index order, then BF16
+    round-to-nearest-even. Returns (float32 sums [n, d], BF16 bits [n, d])."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    a = np.ascontiguousarray(a_bits, dtype=np.uint16)
+    n, d = x.shape
+    assert a.shape == (d, d)
+    acc = np.empty((n, d), dtype=np.float32)
+    out = np.empty((n, d), dtype=np.uint16)
+    if n:
+        lib().oracle_row_transform(n, d, _ptr(x, ctypes.c_uint16), _ptr(a, ctypes.c_uint16),
+                                   _ptr(acc, ctypes.c_float), _ptr(out, ctypes.c_uint16))
+    return acc, out
+
+
+def write_transformed(cfg: Config, c_new, kr_new, cu_new, seq_lens, max_new, page_table, pool, sink, ring,
+                      a_c=None, a_r=None) -> int:
+    """The writer over transformed rows: c A_c and k_R A_R (either may be None: unchanged)."""
+    c = row_transform(c_new, a_c)[1] if a_c is not None else c_new
+    kr = row_transform(kr_new, a_r)[1] if a_r is not None else kr_new
+    return write(cfg, c, kr, cu_new, seq_lens, max_new, page_table, pool, sink, ring)

@@ -552,3 +552,46 @@ int oracle_decode_bf16(int B, int H, const uint16_t* q_lat, const uint16_t* q_ro
   }
   return flags;
 }
+
+/* ---------------------------------------------------------------- cached-tensor transforms */
+
+/* Round a float to BF16, to nearest with ties to even (the upper 16 bits of binary32 after
+   adding half of the dropped part's unit, biased towards the even result); NaN stays NaN. */
+static uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x0040u);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+static float bf16_to_f32(uint16_t bits) {
+  const uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* RAQ-MLA page, Figure 4: before a token is cached, its latent is mapped to c A_c (after the
+   RMSNorm) and its positional key to k_R A_R (after RoPE); the read path compensates with the
+   inverses on the weights / query side, so the cache simply holds the transformed rows.
+   Reading taken (the page fixes no arithmetic): the transform is a BF16 matrix A [dim][dim]
+   applied to a BF16 row x as x'_j = sum_i x_i A[i][j], the sum accumulated in float32 in the
+   order i = 0, 1, ..., dim-1 starting from +0 (a BF16 x BF16 product is exact in float32, so
+   each step rounds once), then rounded to BF16 to nearest-even. acc_out (nullable) receives
+   the float32 sums before that rounding. */
+void oracle_row_transform(int n_rows, int dim, const uint16_t* x, const uint16_t* a, float* acc_out,
+                          uint16_t* out) {
+  for (int r = 0; r < n_rows; ++r) {
+    const uint16_t* xr = x + (size_t)r * dim;
+    for (int j = 0; j < dim; ++j) {
+      float acc = 0.0f;
+      for (int i = 0; i < dim; ++i) {
+        const float prod = bf16_to_f32(xr[i]) * bf16_to_f32(a[(size_t)i * dim + j]);
+        acc = acc + prod;
+      }
+      if (acc_out) acc_out[(size_t)r * dim + j] = acc;
+      out[(size_t)r * dim + j] = f32_to_bf16_rne(acc);
+    }
+  }
+}
