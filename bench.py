@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--sweep-batches", default="1,8,32")
     ap.add_argument("--sweep-heads", type=int, default=16)
     ap.add_argument("--sweep-max-tokens", type=int, default=1 << 20)
+    ap.add_argument("--transform", action="store_true",
+                    help="per-layer cost of the latent transform A_c: standalone kernel vs fused in the writer")
     return ap.parse_args()
 
 
@@ -630,6 +632,92 @@ def run_sweep(args):
     return 0
 
 
+# ------------------------------------------------------------------ latent-transform cost
+
+def run_transform(args):
+    """Per-layer cost of the latent transform A_c at decode batches 1..64 over a 2K-token C4R4
+    cache (16 heads), in the form of the RAQ-MLA page's appendix Table 9: "standalone" is the
+    transform as its own kernel before the cache write, "fused" the extra time of the writer
+    that applies it; "share" is the fused cost relative to the transforming write plus the
+    decode attention. Each operation is captured 20 times in one CUDA graph and the graph
+    replayed (back-to-back calls, caches and A_c L2-resident, as inside a decode step); the
+    writes rewrite the same token slot (lengths are not advanced)."""
+    import torch
+
+    import bit_mla_kv_qcache_gb300 as q
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    T, H, reps, per_graph = 2048, 16, max(10, args.steps), 20
+    stream = torch.cuda.Stream(device=dev)
+    rng = np.random.default_rng(2024)
+    a_c = torch.from_numpy((rng.standard_normal((512, 512)) / math.sqrt(512)).astype(np.float32)).to(
+        torch.bfloat16).view(torch.int16).to(dev)
+    rows = []
+    with ClockSampler(0) as clk:
+        for B in (1, 2, 4, 8, 64):
+            w = workloads.Workload("xf_c4r4", B, H, T, 4, 128)
+            inp = workloads.make_inputs(w, extra_pages=1)
+            to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else
+                                                np.ascontiguousarray(a)).to(dev)
+            cfg = q.make_config(**w.config_kwargs())
+            cache = q.QuantizedMLACache(cfg, B, inp.page_table.shape[1], inp.n_pages,
+                                        page_table=to_dev(inp.page_table), device=dev)
+            cache.write(to_dev(inp.c), to_dev(inp.kr), to_dev(inp.cu), T)
+            c1, k1 = workloads.draw_tokens(rng, B, w.latent_dist, inp.outliers, w.outlier_scale)
+            c_new, kr_new = to_dev(c1), to_dev(k1)
+            c_t = torch.empty_like(c_new)
+            cu1 = torch.arange(B + 1, dtype=torch.int32, device=dev)
+            q_lat, q_rope = to_dev(inp.q_lat), to_dev(inp.q_rope)
+            out = torch.empty((B, H, 512), dtype=torch.float32, device=dev)
+            lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+            ws_buf = cache.workspace(H)
+            ops = {
+                "write": lambda: q.mla_qcache_write(cfg, c_new, kr_new, cu1, cache.seq_lens, 1, cache.page_table,
+                                                    cache.pool, cache.sink, cache.ring, cache.err),
+                "write_fused": lambda: q.mla_qcache_write_transformed(
+                    cfg, c_new, kr_new, cu1, cache.seq_lens, 1, cache.page_table, cache.pool, cache.sink,
+                    cache.ring, cache.err, a_c=a_c),
+                "transform": lambda: q.mla_qcache_row_transform(c_new, a_c, c_t, cache.err),
+                "decode": lambda: q.mla_qcache_decode_attn(cfg, q_lat, q_rope, cache.page_table, cache.seq_lens,
+                                                           cache.pool, cache.sink, cache.ring, w.softmax_scale, out,
+                                                           lse, ws_buf, cache.err),
+            }
+            us = {}
+            with torch.cuda.stream(stream):
+                for name, fn in ops.items():
+                    fn()
+                    torch.cuda.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        for _ in range(per_graph):
+                            fn()
+                    for _ in range(3):
+                        g.replay()
+                    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    s_ev.record(stream)
+                    for _ in range(reps):
+                        g.replay()
+                    e_ev.record(stream)
+                    torch.cuda.synchronize()
+                    us[name] = s_ev.elapsed_time(e_ev) * 1e3 / (reps * per_graph)
+            if cache.error_bits():
+                raise RuntimeError("device error bits set in the transform benchmark")
+            fused = max(0.0, us["write_fused"] - us["write"])
+            rows.append({"batch": B, "standalone_us": us["transform"], "fused_us": fused,
+                         "share": fused / (us["write_fused"] + us["decode"]), "write_us": us["write"],
+                         "write_fused_us": us["write_fused"], "decode_us": us["decode"]})
+            del cache
+            torch.cuda.empty_cache()
+    print(json.dumps({
+        "mode": "latent_transform_cost", "metric": "per-layer cost of the latent transform A_c (512x512 BF16), "
+                                                   "standalone kernel vs fused in the writer",
+        "unit": "us", "cache": "C4R4 page 128 sink 4 recent 128, 2048 tokens, 16 heads",
+        "timing": f"{per_graph} calls per CUDA graph, {reps} replays, L2-resident", "rows": rows,
+        "clocks": clk.summary(), "data": "synthetic"}))
+    return 0
+
+
 def cpu_baseline(w):
     n_seq = max(1, w.batch // 16)
     step, scale = oracle_step_sample(w, n_seq)
@@ -648,6 +736,8 @@ def main():
         return run_reference(args, w)
     if args.sweep:
         return run_sweep(args)
+    if args.transform:
+        return run_transform(args)
     return run_native(args, w)
 
 

@@ -21,7 +21,8 @@ DEV_BAD_PAGE, DEV_SEQ_OVERFLOW, DEV_NONFINITE, DEV_RANGE, DEV_ROWS, DEV_TIMEOUT 
 EXPORTS = ("mla_qcache_page_bytes", "mla_qcache_config_check", "mla_qcache_workspace_bytes",
            "mla_qcache_write", "mla_qcache_decode_attn", "mla_qcache_strerror",
            "mla_qcache_decode_attn_noalloc", "mla_qcache_noalloc_scratch_bytes", "mla_qcache_advance",
-           "mla_qcache_write_advance", "mla_qcache_decode_attn_bf16", "mla_qcache_bf16_workspace_bytes")
+           "mla_qcache_write_advance", "mla_qcache_decode_attn_bf16", "mla_qcache_bf16_workspace_bytes",
+           "mla_qcache_write_transformed", "mla_qcache_row_transform")
 
 
 class Config(ctypes.Structure):
@@ -75,6 +76,11 @@ def lib() -> ctypes.CDLL:
         L.mla_qcache_write_advance.restype = ctypes.c_int
         L.mla_qcache_write_advance.argtypes = [P(Config), i32, i32, vp, vp, vp, vp, vp, i32, vp, i32, vp, i64, vp, vp,
                                                vp, vp]
+        L.mla_qcache_write_transformed.restype = ctypes.c_int
+        L.mla_qcache_write_transformed.argtypes = [P(Config), i32, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp, i32, vp,
+                                                   i64, vp, vp, vp, vp]
+        L.mla_qcache_row_transform.restype = ctypes.c_int
+        L.mla_qcache_row_transform.argtypes = [i32, i32, vp, vp, vp, vp, vp]
         L.mla_qcache_bf16_workspace_bytes.restype = sz
         L.mla_qcache_bf16_workspace_bytes.argtypes = [i32, i32, i32, i32]
         L.mla_qcache_decode_attn_bf16.restype = ctypes.c_int
@@ -155,6 +161,38 @@ def mla_qcache_write_advance(cfg: Config, c_new, kr_new, cu_new, seq_lens, seq_l
         pool.shape[0], _ptr(sink_buf, "sink_buf", 2, allow_none=True) if cfg.n_sink else None,
         _ptr(recent_buf, "recent_buf", 2), _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
     _raise(st, "mla_qcache_write_advance")
+
+
+def mla_qcache_write_transformed(cfg: Config, c_new, kr_new, cu_new, seq_lens, max_new: int, page_table, pool,
+                                 sink_buf, recent_buf, err_word, a_c=None, a_r=None, seq_lens_next=None,
+                                 stream=None) -> None:
+    """The writer over c A_c and k_R A_R (either transform may be None), with the length update
+    when seq_lens_next is given (see include/mla_qcache.h)."""
+    B = seq_lens.shape[0]
+    n_rows = c_new.shape[0]
+    if a_c is not None and tuple(a_c.shape) != (512, 512):
+        raise ValueError(f"a_c must be [512, 512], got {tuple(a_c.shape)}")
+    if a_r is not None and tuple(a_r.shape) != (64, 64):
+        raise ValueError(f"a_r must be [64, 64], got {tuple(a_r.shape)}")
+    st = lib().mla_qcache_write_transformed(
+        ctypes.byref(cfg), B, n_rows, _ptr(c_new, "c_new", 2), _ptr(kr_new, "kr_new", 2),
+        _ptr(cu_new, "cu_new", dtype=torch.int32), _ptr(seq_lens, "seq_lens", dtype=torch.int32),
+        _ptr(seq_lens_next, "seq_lens_next", dtype=torch.int32, allow_none=True), int(max_new),
+        _ptr(a_c, "a_c", 2, allow_none=True), _ptr(a_r, "a_r", 2, allow_none=True),
+        _ptr(page_table, "page_table", dtype=torch.int32), page_table.shape[1], _ptr(pool, "pool", 1),
+        pool.shape[0], _ptr(sink_buf, "sink_buf", 2, allow_none=True) if cfg.n_sink else None,
+        _ptr(recent_buf, "recent_buf", 2), _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
+    _raise(st, "mla_qcache_write_transformed")
+
+
+def mla_qcache_row_transform(x, a, out, err_word, stream=None) -> None:
+    """out = x A for BF16 rows x [n, d] (d = 64 or 512) and A [d, d] (see include/mla_qcache.h)."""
+    n, d = x.shape
+    if tuple(a.shape) != (d, d) or tuple(out.shape) != (n, d):
+        raise ValueError("row_transform: x [n, d], a [d, d], out [n, d]")
+    st = lib().mla_qcache_row_transform(n, d, _ptr(x, "x", 2), _ptr(a, "a", 2), _ptr(out, "out", 2),
+                                        _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
+    _raise(st, "mla_qcache_row_transform")
 
 
 def bf16_workspace_bytes(B: int, H: int, max_pages: int, page_size: int) -> int:

@@ -60,7 +60,8 @@ size_t mla_qcache_workspace_bytes(const mla_qcache_config* cfg, int32_t B, int32
 static int write_impl(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, const uint16_t* c_new,
                      const uint16_t* kr_new, const int32_t* cu_new, const int32_t* seq_lens, int32_t max_new,
                      const int32_t* page_table, int32_t max_pages, uint8_t* pool, int64_t n_pages,
-                     uint16_t* sink_buf, uint16_t* recent_buf, int32_t* err_word, int32_t* seq_next, void* stream) {
+                     uint16_t* sink_buf, uint16_t* recent_buf, int32_t* err_word, int32_t* seq_next, void* stream,
+                     const uint16_t* a_c = nullptr, const uint16_t* a_r = nullptr) {
   int st = check_config(cfg);
   if (st != MLA_QCACHE_OK) return st;
   if (B < 1 || B > (1 << 20) || n_rows < 0 || max_pages < 1 || n_pages < 1) return MLA_QCACHE_ERR_SHAPE;
@@ -74,15 +75,18 @@ static int write_impl(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, c
                : MLA_QCACHE_ERR_CUDA;
   }
   if (max_new < 1) return MLA_QCACHE_ERR_SHAPE;
-  // one CTA per row plus four per page that may fill, in one grid dimension
-  if (static_cast<int64_t>(B) * (max_new / cfg->page_size + 1) * 4 + n_rows > 0x7fffffff)
+  // one CTA per row (a cluster of eight when the rows are transformed, the grid then padded to
+  // whole clusters) plus four per page that may fill, in one grid dimension
+  const int64_t row_ctas = (a_c || a_r) ? static_cast<int64_t>(n_rows) * 8 + 7 : n_rows;
+  if (static_cast<int64_t>(B) * (max_new / cfg->page_size + 1) * 4 + row_ctas > 0x7fffffff)
     return MLA_QCACHE_ERR_SHAPE;
   if (!c_new || !kr_new || !cu_new || !seq_lens || !page_table || !pool || !recent_buf || !err_word)
     return MLA_QCACHE_ERR_NULL;
   if (cfg->n_sink > 0 && !sink_buf) return MLA_QCACHE_ERR_NULL;
   if (!aligned(c_new, 16) || !aligned(kr_new, 4) || !aligned(pool, 16) || !aligned(recent_buf, 16) ||
       (sink_buf && !aligned(sink_buf, 16)) || !aligned(cu_new, 4) || !aligned(seq_lens, 4) ||
-      !aligned(page_table, 4) || !aligned(err_word, 4) || (seq_next && !aligned(seq_next, 4)))
+      !aligned(page_table, 4) || !aligned(err_word, 4) || (seq_next && !aligned(seq_next, 4)) ||
+      (a_c && !aligned(a_c, 16)) || (a_r && !aligned(a_r, 16)))
     return MLA_QCACHE_ERR_ALIGN;
 
   mlaq::WriteParams p{};
@@ -111,7 +115,9 @@ static int write_impl(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, c
   p.ring = recent_buf;
   p.err = err_word;
   p.seq_next = seq_next;
-  const int token_blocks = n_rows;  // one CTA per new token
+  p.a_c = a_c;
+  p.a_r = a_r;
+  const int token_blocks = n_rows;  // one CTA (or cluster) per new token
   const int fill_per_seq = max_new / p.P + 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -158,6 +164,34 @@ int mla_qcache_write_advance(const mla_qcache_config* cfg, int32_t B, int32_t n_
   }
   return write_impl(cfg, B, n_rows, c_new, kr_new, cu_new, seq_lens, max_new, page_table, max_pages, pool, n_pages,
                     sink_buf, recent_buf, err_word, seq_lens_next, stream);
+}
+
+int mla_qcache_write_transformed(const mla_qcache_config* cfg, int32_t B, int32_t n_rows, const uint16_t* c_new,
+                                 const uint16_t* kr_new, const int32_t* cu_new, const int32_t* seq_lens,
+                                 int32_t* seq_lens_next, int32_t max_new, const uint16_t* a_c, const uint16_t* a_r,
+                                 const int32_t* page_table, int32_t max_pages, uint8_t* pool, int64_t n_pages,
+                                 uint16_t* sink_buf, uint16_t* recent_buf, int32_t* err_word, void* stream) {
+  if (seq_lens_next && B >= 1 && seq_lens) {  // the two length arrays must not overlap
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(seq_lens), b0 = reinterpret_cast<uintptr_t>(seq_lens_next);
+    const uintptr_t len = static_cast<uintptr_t>(B) * sizeof(int32_t);
+    if (a0 < b0 + len && b0 < a0 + len) return MLA_QCACHE_ERR_SHAPE;
+  }
+  return write_impl(cfg, B, n_rows, c_new, kr_new, cu_new, seq_lens, max_new, page_table, max_pages, pool, n_pages,
+                    sink_buf, recent_buf, err_word, seq_lens_next, stream, a_c, a_r);
+}
+
+int mla_qcache_row_transform(int32_t n_rows, int32_t dim, const uint16_t* x, const uint16_t* a, uint16_t* out,
+                             int32_t* err_word, void* stream) {
+  if (n_rows < 0 || (dim != 64 && dim != 512)) return MLA_QCACHE_ERR_SHAPE;
+  if (n_rows == 0) return MLA_QCACHE_OK;
+  if (!x || !a || !out || !err_word) return MLA_QCACHE_ERR_NULL;
+  if (!aligned(x, 2) || !aligned(a, 16) || !aligned(out, 2) || !aligned(err_word, 4)) return MLA_QCACHE_ERR_ALIGN;
+  const uintptr_t xs = reinterpret_cast<uintptr_t>(x), os = reinterpret_cast<uintptr_t>(out);
+  const uintptr_t len = static_cast<uintptr_t>(n_rows) * static_cast<uintptr_t>(dim) * 2;
+  if (xs < os + len && os < xs + len) return MLA_QCACHE_ERR_SHAPE;  // in place is not supported
+  const cudaError_t e =
+      mlaq::launch_row_transform(n_rows, dim, x, a, out, err_word, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
 }
 
 int mla_qcache_advance(const int32_t* cu_new, int32_t* seq_lens, int32_t B, void* stream) {

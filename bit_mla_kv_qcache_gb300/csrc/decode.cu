@@ -1290,12 +1290,16 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
 int decode_bf16_num_parts(int B, int H, int max_pages, int P, int num_sms) {
   const int groups = B * (H / 16);
   int ns = kCtasPerSm * num_sms / (groups > 0 ? groups : 1);
+  if (ns < 1) ns = 1;
   const long long max_tiles = (static_cast<long long>(max_pages) * P + kTile - 1) / kTile;
   // Few sequence-head groups already fill the GPU with one wave of shares; only where one wave
   // leaves a share well above ~128 16-token tiles (many groups, long tables) are shares made
-  // smaller, at the price of several waves.
+  // smaller: a whole number of waves (at most 8), so that no partial wave trails the last.
   const long long by_len = (max_tiles + 127) / 128;
-  if (by_len > 2LL * ns) ns = static_cast<int>(by_len > 512 ? 512 : by_len);
+  if (by_len > 2LL * ns) {
+    const long long waves = (by_len + ns - 1) / ns;
+    ns = static_cast<int>((waves > 8 ? 8 : waves) * ns);
+  }
   if (ns > max_tiles) ns = static_cast<int>(max_tiles);
   if (ns < 1) ns = 1;
   return ns;

@@ -35,12 +35,17 @@ struct WriteParams {
   uint16_t* ring;
   int32_t* err;
   int32_t* seq_next;  // optional: lengths after the call (written by page-fill CTA 0 of each sequence)
+  const uint16_t* a_c;  // optional BF16 [512][512]: the latent is cached as c A_c
+  const uint16_t* a_r;  // optional BF16 [64][64]: k_R is cached as k_R A_R
   int token_blocks;  // blocks [0, token_blocks) do per-token work (one token per block)
   int fill_per_seq;  // page-fill blocks per sequence after the token blocks
 };
 
 // One launch doing per-token packing/retention (token_blocks > 0) and/or page fills.
 cudaError_t launch_write(const WriteParams& p, cudaStream_t stream);
+// out = x A row by row (BF16 rows of dim 64 or 512), the arithmetic of the transforming writer.
+cudaError_t launch_row_transform(int n_rows, int dim, const uint16_t* x, const uint16_t* a, uint16_t* out,
+                                 int32_t* err, cudaStream_t stream);
 // seq_lens[b] += cu_new[b+1] - cu_new[b] for b in [0, B).
 cudaError_t launch_advance(const int32_t* cu_new, int32_t* seq_lens, int B, cudaStream_t stream);
 

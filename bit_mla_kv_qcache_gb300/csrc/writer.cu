@@ -9,6 +9,17 @@
 // Every code is decided exactly: the nearest level is found from a float estimate and then
 // confirmed against the exact midpoints min + (j + 1/2) * scale, which are formed without
 // rounding (in float when a directed-rounding pair agrees, else in double).
+//
+// With the cached-tensor transforms of the RAQ-MLA page (Figure 4: A_c on the latent, A_R on
+// k_R) the writer caches x A in place of x: each token is then served by a cluster of eight
+// CTAs that form 64 transformed latent channels each (their 64-column slice of A_c arrives by
+// tensor-map copies) and hand them to the cluster's first CTA through distributed shared
+// memory; page fills transform the k_R of the call's new tokens.
+#include <cooperative_groups.h>
+#include <cstring>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "kernels.cuh"
@@ -96,10 +107,179 @@ __device__ __forceinline__ int find_seq(const int32_t* cu, int B, int r) {
   return lo;
 }
 
+// ------------------------------------------------------------------ cached-tensor transforms
+// x'_j = sum_i x_i A[i][j] for a BF16 row x and a BF16 matrix A [dim][dim] (row-major): the
+// float32 sum runs over i = 0, 1, ..., dim-1 from +0, one rounded product (exact for two BF16
+// values) and one rounded addition per step (this file is built without contraction), and is
+// rounded to BF16 to nearest-even.
+constexpr int kXfCtas = 8;  // CTAs (one cluster) per token when rows are transformed
+
+__device__ __forceinline__ float bf16_bits_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+__device__ __forceinline__ uint16_t f32_bf16_bits(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+
+// The CTA's slice of a latent transform (columns col0 .. col0 + 63 of a [512][512]) arrives in
+// shared memory as four tensor-map boxes of 128 rows x 64 columns (16 KB each, all in flight at
+// once, one barrier each); thread tid < 64 runs the sum of column col0 + tid over the rows in
+// order as the boxes land. A_R ([64][64], 8 KB, contiguous) is one bulk copy. Every wait is
+// bounded; a wait that gives up is agreed on by the whole CTA, the copies still in flight are
+// waited for (bounded), and false is returned.
+constexpr int kXfCols = kLatent / kXfCtas;                    // 64 columns per CTA
+constexpr int kXfBlockRows = 128;                             // rows per box
+constexpr int kXfBlocks = kLatent / kXfBlockRows;             // 4
+constexpr int kXfBoxBytes = kXfBlockRows * kXfCols * 2;       // 16 KB
+constexpr int kXfRopeOff = kXfBlocks * kXfBoxBytes;           // A_R after the boxes
+constexpr int kXfSmemBytes = kXfRopeOff + kRope * kRope * 2;  // 72 KB of dynamic shared memory
+constexpr int kXfBars = kXfBlocks + 1;                        // one per box, one for A_R
+constexpr long long kXfWaitBudget = 4ll << 30;                // ~2 s at 2 GHz
+
+__device__ __forceinline__ void xf_bars_init(uint64_t* bars) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kXfBars; ++i) mbar_init(bars + i, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Thread 0 requests A_R (one copy) into the bytes after the boxes.
+__device__ __forceinline__ void xf_issue_rope(const uint16_t* a_r, uint8_t* smem, uint64_t* bar) {
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(bar, kRope * kRope * 2);
+    bulk_g2s(smem + kXfRopeOff, a_r, kRope * kRope * 2, bar);
+  }
+}
+
+// Thread 0 requests the four boxes of columns col0 .. col0 + 63 (col0 * 2 bytes is a multiple of 16).
+__device__ __forceinline__ void xf_issue_latent(const CUtensorMap* map, int col0, uint8_t* smem, uint64_t* bars) {
+  if (threadIdx.x == 0) {
+    for (int rb = 0; rb < kXfBlocks; ++rb) {
+      mbar_arrive_expect_tx(bars + rb, kXfBoxBytes);
+      tma_load_2d(smem + rb * kXfBoxBytes, map, col0, rb * kXfBlockRows, bars + rb);
+    }
+  }
+}
+
+__device__ bool latent_slice_transform(const float* s_x, const uint8_t* smem, uint64_t* bars, uint16_t& out) {
+  float acc = 0.f;
+  for (int rb = 0; rb < kXfBlocks; ++rb) {
+    const bool ok = mbar_wait_bounded(bars + rb, 0, kXfWaitBudget);
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0)
+        for (int j = rb; j < kXfBlocks; ++j) (void)mbar_wait_bounded(bars + j, 0, kXfWaitBudget >> 4);
+      return false;
+    }
+    if (threadIdx.x < kXfCols) {
+      const uint16_t* blk = reinterpret_cast<const uint16_t*>(smem + rb * kXfBoxBytes) + threadIdx.x;
+      const float* xb = s_x + rb * kXfBlockRows;
+#pragma unroll 16
+      for (int i = 0; i < kXfBlockRows; ++i) acc = acc + xb[i] * bf16_bits_f32(blk[i * kXfCols]);
+    }
+  }
+  out = f32_bf16_bits(acc);
+  return true;
+}
+
+// Channel j < 64 of k_R A_R from the staged A_R (the CTA waits for it first).
+__device__ bool rope_transform(const float* s_k, const uint8_t* smem, uint64_t* bar, int j, uint16_t& out) {
+  const bool ok = mbar_wait_bounded(bar, 0, kXfWaitBudget);
+  if (__syncthreads_or(!ok)) {
+    if (threadIdx.x == 0) (void)mbar_wait_bounded(bar, 0, kXfWaitBudget >> 4);
+    return false;
+  }
+  if (j < kRope) {
+    const uint16_t* ar = reinterpret_cast<const uint16_t*>(smem + kXfRopeOff) + j;
+    float acc = 0.f;
+#pragma unroll 16
+    for (int i = 0; i < kRope; ++i) acc = acc + s_k[i] * bf16_bits_f32(ar[i * kRope]);
+    out = f32_bf16_bits(acc);
+  }
+  return true;
+}
+
+// Channels j and j+1 (j even) of k_R A_R for one k_R row in global memory, A_R staged in shared
+// memory (page fills of the call's new tokens).
+__device__ __forceinline__ uint32_t transform_rope_pair(const uint16_t* x, const uint16_t* ar, int j) {
+  uint32_t xv[kRope / 2];  // the row's 32-bit words, all loads in flight together (rows are 4-byte aligned)
+#pragma unroll
+  for (int v = 0; v < kRope / 2; ++v) xv[v] = __ldg(reinterpret_cast<const uint32_t*>(x) + v);
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRope; ++i) {
+    const float xi = (i & 1) ? bf16_hi(xv[i >> 1]) : bf16_lo(xv[i >> 1]);
+    const uint32_t av = *reinterpret_cast<const uint32_t*>(ar + i * kRope + j);
+    a0 = a0 + xi * bf16_lo(av);
+    a1 = a1 + xi * bf16_hi(av);
+  }
+  return static_cast<uint32_t>(f32_bf16_bits(a0)) | (static_cast<uint32_t>(f32_bf16_bits(a1)) << 16);
+}
+
+// The cluster of token row r: CTA `rank` forms latent channels 64 rank .. 64 rank + 63 (one per
+// thread of its first two warps), CTA 1 also the 64 k_R channels; after the cluster barrier the
+// first CTA gathers the row in the per-token layout (thread: latent channels 4 tid .. 4 tid + 3;
+// warp-0 lanes: k_R channels 2 lane, 2 lane + 1). Every CTA of the cluster passes both barriers.
+__device__ void transform_token(const WriteParams& p, const CUtensorMap* a_map, int r, uint8_t* smem, uint2& cv,
+                                uint32_t& kr2) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = static_cast<int>(cl.block_rank());
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __shared__ float s_x[kRow];
+  __shared__ __align__(16) uint16_t s_y[kXfCols + kRope];
+  __shared__ __align__(8) uint64_t bars[kXfBars];
+  xf_bars_init(bars);
+  const bool rope_here = rank == 1 && p.a_r != nullptr;
+  if (p.a_c) xf_issue_latent(a_map, kXfCols * rank, smem, bars);
+  if (rope_here) xf_issue_rope(p.a_r, smem, bars + kXfBlocks);
+  const uint16_t* c_row = p.c_new + static_cast<size_t>(r) * kLatent;
+  const uint16_t* k_row = p.kr_new + static_cast<size_t>(r) * kRope;
+  const uint2 raw = __ldg(reinterpret_cast<const uint2*>(c_row) + tid);
+  s_x[4 * tid] = bf16_lo(raw.x);
+  s_x[4 * tid + 1] = bf16_hi(raw.x);
+  s_x[4 * tid + 2] = bf16_lo(raw.y);
+  s_x[4 * tid + 3] = bf16_hi(raw.y);
+  if (tid < kRope / 2) {
+    const uint32_t k = __ldg(reinterpret_cast<const uint32_t*>(k_row) + tid);
+    s_x[kLatent + 2 * tid] = bf16_lo(k);
+    s_x[kLatent + 2 * tid + 1] = bf16_hi(k);
+  }
+  __syncthreads();
+  bool ok = true;
+  uint16_t y = tid < kXfCols ? __ldg(c_row + kXfCols * rank + tid) : 0;
+  if (p.a_c) ok = latent_slice_transform(s_x, smem, bars, y);
+  if (tid < kXfCols) s_y[tid] = y;
+  if (rank == 1 && tid < kRope) s_y[kXfCols + tid] = __ldg(k_row + tid);
+  if (rope_here) {
+    uint16_t yr = 0;
+    if (rope_transform(s_x + kLatent, smem, bars + kXfBlocks, tid, yr)) {
+      if (tid < kRope) s_y[kXfCols + tid] = yr;
+    } else {
+      ok = false;
+    }
+  }
+  if (!ok && tid == 0) raise_err(p.err, kErrTimeout);
+  cl.sync();  // every slice written
+  if (rank == 0) {
+    // channel 4 tid lives in CTA 4 tid / 64
+    const uint16_t* src = cl.map_shared_rank(s_y, (4 * tid) / kXfCols);
+    cv = *reinterpret_cast<const uint2*>(src + ((4 * tid) & (kXfCols - 1)));
+    if (warp == 0) kr2 = *reinterpret_cast<const uint32_t*>(cl.map_shared_rank(s_y, 1) + kXfCols + 2 * lane);
+  }
+  cl.sync();  // the slices stay in place until the first CTA has read them
+}
+
 // ------------------------------------------------------------------ per-token work (one CTA)
 // 128 threads per new token: warp w owns latent group w (channels 128w..128w+127, four per
 // lane); lanes of warp 0 also carry the token's k_R (two channels each) for the retention copy.
-__device__ void write_token(const WriteParams& p, int r, int (&s_cnt)[2][4]) {
+// kGiven: the row arrives in cv / kr2 (transformed by the token's cluster) instead of from c_new.
+template <bool kGiven>
+__device__ void write_token(const WriteParams& p, int r, int (&s_cnt)[2][4], uint2 cv, uint32_t kr2) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // decode steps write one row per sequence (cu_new[b] = b): then row r belongs to sequence r,
   // found with two independent loads instead of a dependent binary search
@@ -128,9 +308,10 @@ __device__ void write_token(const WriteParams& p, int r, int (&s_cnt)[2][4]) {
   const int64_t t_final = static_cast<int64_t>(s0) + n_b;
 
   // ---- load: thread holds latent channels [4*tid, 4*tid+4); warp 0 lanes k_R [2*lane, 2*lane+2)
-  const uint2 cv = __ldg(reinterpret_cast<const uint2*>(p.c_new + static_cast<size_t>(r) * kLatent) + tid);
-  uint32_t kr2 = 0;
-  if (warp == 0) kr2 = __ldg(reinterpret_cast<const uint32_t*>(p.kr_new + static_cast<size_t>(r) * kRope) + lane);
+  if constexpr (!kGiven) {
+    cv = __ldg(reinterpret_cast<const uint2*>(p.c_new + static_cast<size_t>(r) * kLatent) + tid);
+    if (warp == 0) kr2 = __ldg(reinterpret_cast<const uint32_t*>(p.kr_new + static_cast<size_t>(r) * kRope) + lane);
+  }
 
   // ---- BF16 retention (pre-quantization values)
   if (t < p.S) {
@@ -248,6 +429,7 @@ __host__ __device__ constexpr size_t fill_smem_floats(int P) {
   return static_cast<size_t>(P) * kFillStride + 2 * kFillSubsets * kFillCh + 3 * kFillCh;
 }
 
+template <bool kTransform>
 __device__ void fill_page(const WriteParams& p, int b, int f, int rr, float* smem) {
   const int tid = threadIdx.x;
   const int r0 = __ldg(p.cu_new + b), r1 = __ldg(p.cu_new + b + 1);
@@ -265,6 +447,16 @@ __device__ void fill_page(const WriteParams& p, int b, int f, int rr, float* sme
   float* red = vals + static_cast<size_t>(P) * kFillStride;  // [2][kFillSubsets][kFillCh]
   float* stats = red + 2 * kFillSubsets * kFillCh;           // [kFillCh][3]
 
+  // A_R for the new tokens' k_R (after the staged values, 16-byte aligned for P % 32 == 0)
+  const uint16_t* ar_s = reinterpret_cast<const uint16_t*>(smem + fill_smem_floats(P));
+  if constexpr (kTransform) {
+    if (p.a_r) {
+      uint4* dst = reinterpret_cast<uint4*>(smem + fill_smem_floats(P));
+      for (int v = threadIdx.x; v < kRope * kRope / 8; v += blockDim.x)
+        dst[v] = __ldg(reinterpret_cast<const uint4*>(p.a_r) + v);
+      __syncthreads();
+    }
+  }
   // gather this CTA's 32 bytes of every token of the page (earlier tokens from the ring, new
   // ones from the input), all loads of a thread in flight together; the page id is checked
   // after them (the loads do not depend on it)
@@ -279,10 +471,18 @@ __device__ void fill_page(const WriteParams& p, int b, int f, int rr, float* sme
       const int u = i >> 3, e = i & 7;
       const int64_t tt = pg * P + u;
       const uint32_t* src;
-      if (tt < s0)
+      if (tt < s0) {
         src = reinterpret_cast<const uint32_t*>(p.ring + (static_cast<size_t>(b) * p.W + (tt % p.W)) * kRow + kLatent);
-      else
-        src = reinterpret_cast<const uint32_t*>(p.kr_new + static_cast<size_t>(r0 + (tt - s0)) * kRope);
+      } else {
+        const uint16_t* k_row = p.kr_new + static_cast<size_t>(r0 + (tt - s0)) * kRope;
+        if constexpr (kTransform) {
+          if (p.a_r) {  // a new token's k_R is cached as k_R A_R
+            w[it] = transform_rope_pair(k_row, ar_s, kFillCh * rr + 2 * e);
+            continue;
+          }
+        }
+        src = reinterpret_cast<const uint32_t*>(k_row);
+      }
       w[it] = __ldg(src + kFillCh / 2 * rr + e);
     }
   }
@@ -353,22 +553,91 @@ __device__ void fill_page(const WriteParams& p, int b, int f, int rr, float* sme
   if (flags && tid == 0) raise_err(p.err, flags);
 }
 
-__global__ void __launch_bounds__(128) write_kernel(const WriteParams p) {
-  extern __shared__ float smem_f[];
+// Blocks [0, token_blocks x per-token CTAs) serve the new rows, the rest the page fills.
+template <bool kTransform>
+__device__ __forceinline__ void write_body(const WriteParams& p, const CUtensorMap* a_map) {
+  extern __shared__ __align__(128) float smem_f[];
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     if (__ldg(p.cu_new) != 0 || __ldg(p.cu_new + p.B) != p.n_rows) raise_err(p.err, kErrRows);
   }
-  if (static_cast<int>(blockIdx.x) < p.token_blocks) {
+  constexpr int kPerToken = kTransform ? kXfCtas : 1;
+  if (static_cast<int>(blockIdx.x) < p.token_blocks * kPerToken) {
     __shared__ int s_cnt[2][4];
-    write_token(p, blockIdx.x, s_cnt);
+    if constexpr (kTransform) {
+      const int r = blockIdx.x / kXfCtas;
+      uint2 cv = make_uint2(0u, 0u);
+      uint32_t kr2 = 0;
+      transform_token(p, a_map, r, reinterpret_cast<uint8_t*>(smem_f), cv, kr2);
+      if (blockIdx.x % kXfCtas != 0) return;  // the cluster's first CTA writes the token
+      write_token<true>(p, r, s_cnt, cv, kr2);
+    } else {
+      write_token<false>(p, blockIdx.x, s_cnt, make_uint2(0u, 0u), 0u);
+    }
     return;
   }
-  const int idx = blockIdx.x - p.token_blocks;
+  const int idx = blockIdx.x - p.token_blocks * kPerToken;
   const int per_seq = p.fill_per_seq * kFillSplit;
+  if (per_seq == 0) return;  // a padding CTA of a launch without page fills
   const int b = idx / per_seq, f = (idx % per_seq) / kFillSplit, rr = idx % kFillSplit;
-  if (b < p.B) fill_page(p, b, f, rr, smem_f);
+  if (b < p.B) fill_page<kTransform>(p, b, f, rr, smem_f);
 }
 
+__global__ void __launch_bounds__(128) write_kernel(const WriteParams p) { write_body<false>(p, nullptr); }
+
+// Rows transformed on the way in: clusters of eight CTAs along x (token clusters, then the fill
+// CTAs, padded to whole clusters with CTAs past the last sequence, which exit).
+__global__ void __cluster_dims__(kXfCtas, 1, 1) __launch_bounds__(128)
+    write_xf_kernel(const WriteParams p, const __grid_constant__ CUtensorMap a_map) {
+  write_body<true>(p, &a_map);
+}
+
+// Standalone transform: CTA (row, part) forms channels 64 part .. 64 part + 63 of one row (all
+// 64 for dim 64), with the arithmetic and staging of the fused writer, so either route caches
+// the same bits.
+__global__ void __launch_bounds__(128) row_transform_kernel(int dim, const uint16_t* x, const uint16_t* a,
+                                                            uint16_t* out, int32_t* err,
+                                                            const __grid_constant__ CUtensorMap a_map) {
+  extern __shared__ __align__(128) uint8_t xf_smem[];
+  __shared__ float s_x[kLatent];
+  __shared__ __align__(8) uint64_t bars[kXfBars];
+  xf_bars_init(bars);
+  const size_t r = blockIdx.x;
+  if (dim == kRope) xf_issue_rope(a, xf_smem, bars + kXfBlocks);
+  else xf_issue_latent(&a_map, kXfCols * blockIdx.y, xf_smem, bars);
+  for (int i = threadIdx.x; i < dim; i += 128) s_x[i] = bf16_bits_f32(__ldg(x + r * dim + i));
+  __syncthreads();
+  uint16_t y = 0;
+  const bool ok = dim == kRope ? rope_transform(s_x, xf_smem, bars + kXfBlocks, threadIdx.x, y)
+                               : latent_slice_transform(s_x, xf_smem, bars, y);
+  if (!ok) {
+    if (threadIdx.x == 0) raise_err(err, kErrTimeout);
+    return;
+  }
+  const int j = (dim == kRope ? 0 : kXfCols * static_cast<int>(blockIdx.y)) + static_cast<int>(threadIdx.x);
+  if (threadIdx.x < (dim == kRope ? kRope : kXfCols)) out[r * dim + j] = y;
+}
+
+// Tensor map of a BF16 [512][512] row-major matrix for boxes of 128 rows x 64 columns (the
+// encoder comes from the driver through the runtime, so nothing links against libcuda).
+cudaError_t encode_latent_map(const uint16_t* a, CUtensorMap* map) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kLatent), static_cast<cuuint64_t>(kLatent)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kLatent) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kXfCols), static_cast<cuuint32_t>(kXfBlockRows)};
+  const cuuint32_t elem[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(a), dims, strides, box, elem,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 __global__ void __launch_bounds__(256) advance_kernel(const int32_t* cu_new, int32_t* seq_lens, int B) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
@@ -383,11 +652,57 @@ cudaError_t launch_advance(const int32_t* cu_new, int32_t* seq_lens, int B, cuda
 }
 
 cudaError_t launch_write(const WriteParams& p, cudaStream_t stream) {
-  const int64_t blocks = p.token_blocks + static_cast<int64_t>(p.B) * p.fill_per_seq * kFillSplit;
+  const bool xf = p.a_c != nullptr || p.a_r != nullptr;
+  int64_t blocks = static_cast<int64_t>(p.token_blocks) * (xf ? kXfCtas : 1) +
+                   static_cast<int64_t>(p.B) * p.fill_per_seq * kFillSplit;
   if (blocks == 0) return cudaSuccess;
+  if (xf) blocks = (blocks + kXfCtas - 1) / kXfCtas * kXfCtas;  // whole clusters
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const size_t smem = p.fill_per_seq > 0 ? fill_smem_floats(p.P) * sizeof(float) : 0;  // <= 10 KB
-  write_kernel<<<static_cast<unsigned>(blocks), 128, smem, stream>>>(p);
+  if (xf) {
+    CUtensorMap a_map;
+    memset(&a_map, 0, sizeof a_map);
+    if (p.a_c != nullptr) {
+      const cudaError_t em = encode_latent_map(p.a_c, &a_map);
+      if (em != cudaSuccess) return em;
+    }
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_done[dev]) {
+      e = cudaFuncSetAttribute(write_xf_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kXfSmemBytes);
+      if (e != cudaSuccess) return e;
+      attr_done[dev] = true;
+    }
+    const size_t fill_xf = p.fill_per_seq > 0 ? fill_smem_floats(p.P) * sizeof(float) + kRope * kRope * 2 : 0;
+    const size_t smem_xf = p.token_blocks > 0 ? static_cast<size_t>(kXfSmemBytes) : 0;
+    write_xf_kernel<<<static_cast<unsigned>(blocks), 128, smem_xf > fill_xf ? smem_xf : fill_xf, stream>>>(p, a_map);
+  } else {
+    write_kernel<<<static_cast<unsigned>(blocks), 128, smem, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_transform(int n_rows, int dim, const uint16_t* x, const uint16_t* a, uint16_t* out,
+                                 int32_t* err, cudaStream_t stream) {
+  if (n_rows == 0) return cudaSuccess;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev]) {
+    e = cudaFuncSetAttribute(row_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kXfSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  CUtensorMap a_map;
+  memset(&a_map, 0, sizeof a_map);
+  if (dim == kLatent && (e = encode_latent_map(a, &a_map)) != cudaSuccess) return e;
+  row_transform_kernel<<<dim3(static_cast<unsigned>(n_rows), dim == kLatent ? kXfCtas : 1), 128, kXfSmemBytes,
+                         stream>>>(dim, x, a, out, err, a_map);
   return cudaGetLastError();
 }
 

@@ -223,6 +223,48 @@ int mla_qcache_write_advance(const mla_qcache_config* cfg, int32_t B, int32_t n_
                              int32_t* err_word, void* stream);
 
 /*
+ * Cache writer over transformed rows (RAQ-MLA page, Figure 4: the latent is cached in the basis
+ * of an invertible A_c, applied after the RMSNorm, and k_R in that of A_R, applied after RoPE;
+ * the read path folds A_c^-1 into the up-projections and compensates k_R on the query side).
+ * Exactly mla_qcache_write (or mla_qcache_write_advance when seq_lens_next is not NULL) of the
+ * rows c A_c and k_R A_R in place of c and k_R, in one launch ("fused", RAQ-MLA page, appendix
+ * Table 9): the page bytes, the BF16 sink/recent rows and the error bits are those that writer
+ * stores for the transformed rows.
+ *   a_c   NULL or BF16 [512][512] row-major, 16-byte aligned: latent channel j is cached as
+ *         the BF16 value of sum_i c_i a_c[i][j].
+ *   a_r   NULL or BF16 [64][64] row-major, 16-byte aligned: the same for k_R.
+ * Arithmetic (the page fixes none; this is the reading taken): each sum is accumulated in
+ * float32 in the order i = 0, 1, ... starting from +0, one rounded product (exact for two BF16
+ * values) and one rounded addition per step, and rounded to BF16 to nearest-even; every
+ * transformed value, and so every code, is therefore reproducible bit for bit.
+ * Each new row is served by a cluster of eight CTAs (64 transformed latent channels each; the
+ * CTA's 64-column slice of a_c arrives in shared memory by tensor-map copies). A copy wait that
+ * gives up sets MLA_QCACHE_DEV_TIMEOUT (the row is then not valid).
+ * Errors: those of mla_qcache_write / mla_qcache_write_advance; misaligned a_c / a_r ->
+ * MLA_QCACHE_ERR_ALIGN; 8 * n_rows + 4 * B * (max_new / P + 1) + 7 above 2^31 - 1 ->
+ * MLA_QCACHE_ERR_SHAPE. A transformed value that overflows sets MLA_QCACHE_DEV_NONFINITE.
+ */
+int mla_qcache_write_transformed(const mla_qcache_config* cfg, int32_t B, int32_t n_rows,
+                                 const uint16_t* c_new, const uint16_t* kr_new, const int32_t* cu_new,
+                                 const int32_t* seq_lens, int32_t* seq_lens_next, int32_t max_new,
+                                 const uint16_t* a_c, const uint16_t* a_r, const int32_t* page_table,
+                                 int32_t max_pages, uint8_t* pool, int64_t n_pages, uint16_t* sink_buf,
+                                 uint16_t* recent_buf, int32_t* err_word, void* stream);
+
+/*
+ * Standalone transform ("standalone", RAQ-MLA page, appendix Table 9: A_c as its own kernel
+ * before the cache write): out[r] = x[r] A for n_rows BF16 rows of dim 64 or 512, with the
+ * arithmetic of mla_qcache_write_transformed (so transforming first and then calling
+ * mla_qcache_write caches the same bytes). x, out: device BF16, 2-byte aligned; a: 16-byte
+ * aligned; out must not overlap x. One CTA per row and 64 output channels. err_word: device
+ * int32, 4-byte aligned; a copy wait that gives up ORs MLA_QCACHE_DEV_TIMEOUT into it.
+ * Errors: dim not 64 / 512 or n_rows < 0 or overlap -> MLA_QCACHE_ERR_SHAPE; NULL ->
+ * MLA_QCACHE_ERR_NULL; misaligned -> MLA_QCACHE_ERR_ALIGN; n_rows == 0 runs nothing.
+ */
+int mla_qcache_row_transform(int32_t n_rows, int32_t dim, const uint16_t* x, const uint16_t* a, uint16_t* out,
+                             int32_t* err_word, void* stream);
+
+/*
  * Length update after a write (the pages leave the bookkeeping to the caller): for every
  * sequence b in [0, B), seq_lens[b] += cu_new[b+1] - cu_new[b], in one kernel on `stream`,
  * ordered after a preceding mla_qcache_write on the same stream. cu_new [B+1] and seq_lens [B]

@@ -109,6 +109,36 @@ def test_host_validation_without_gpu(L):
                                         1, p, 1, p, p, p, None) == -2
 
 
+def test_transform_entry_points_validate_on_the_host(L):
+    lib = L.lib()
+    cfg = L.make_config(4, 128)
+    p, p2 = ctypes.c_void_p(16 * 1024), ctypes.c_void_p(64 * 1024)
+    odd = ctypes.c_void_p(16 * 1024 + 2)
+
+    def wt(a_c, a_r, nxt=None, B=4, lens=p, n_rows=4):
+        return lib.mla_qcache_write_transformed(ctypes.byref(cfg), B, n_rows, p, p, p, lens, nxt, 1, a_c, a_r, p, 1,
+                                                p, 1, p, p, p, None)
+
+    assert wt(odd, None) == -4 and wt(None, odd) == -4  # transforms need 16-byte alignment
+    assert wt(ctypes.c_void_p(16 * 1024 + 8), None) == -4
+    assert wt(p, p, nxt=p) == -3  # overlapping length arrays
+    assert wt(p, p, nxt=ctypes.c_void_p(32 * 1024 + 2)) == -4
+    assert wt(p, p, B=0) == -3
+    # eight CTAs per transformed row count against the grid limit
+    assert lib.mla_qcache_write_transformed(ctypes.byref(cfg), 1, (1 << 28) + 8, p, p, p, p, None, 1, p, None, p, 1,
+                                            p, 1, p, p, p, None) == -3
+    # standalone transform: dim, sizes, pointers, alignment, overlap
+    e = ctypes.c_void_p(128 * 1024)
+    assert lib.mla_qcache_row_transform(4, 128, p, p, p2, e, None) == -3
+    assert lib.mla_qcache_row_transform(-1, 512, p, p, p2, e, None) == -3
+    assert lib.mla_qcache_row_transform(0, 512, None, None, None, None, None) == 0
+    assert lib.mla_qcache_row_transform(4, 512, None, p, p2, e, None) == -1
+    assert lib.mla_qcache_row_transform(4, 512, p, p, p2, None, None) == -1
+    assert lib.mla_qcache_row_transform(4, 512, ctypes.c_void_p(16 * 1024 + 1), p, p2, e, None) == -4
+    assert lib.mla_qcache_row_transform(4, 512, p, ctypes.c_void_p(16 * 1024 + 4), p2, e, None) == -4  # a: 16 B
+    assert lib.mla_qcache_row_transform(4, 512, p, p, ctypes.c_void_p(16 * 1024 + 2048), e, None) == -3  # overlaps x
+
+
 def test_product_path_has_no_cpu_fallback(L, monkeypatch):
     """Without the built library the binding raises instead of computing anything else."""
     import bit_mla_kv_qcache_gb300.binding as b
