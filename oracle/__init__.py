@@ -15,7 +15,8 @@ effective-bits figures of Table 5, closed forms of softmax attention,
 ``torch.nn.functional.scaled_dot_product_attention`` in float64, and for the cached-tensor
 transform: identity and signed-permutation closed forms, a hand-worked float32 sum that fixes
 the accumulation order, torch's float64 matmul within the float32 summation bound, and torch's
-BF16 rounding).
+BF16 rounding; for the projections either side of attention: identity, per-head scaled and
+single-entry weights, a hand-worked product, and the BF16 rounding of the attention output).
 """
 from __future__ import annotations
 
@@ -276,3 +277,63 @@ def write_transformed(cfg: Config, c_new, kr_new, cu_new, seq_lens, max_new, pag
     c = row_transform(c_new, a_c)[1] if a_c is not None else c_new
     kr = row_transform(kr_new, a_r)[1] if a_r is not None else kr_new
     return write(cfg, c, kr, cu_new, seq_lens, max_new, page_table, pool, sink, ring)
+
+
+# ------------------------------------------------------------------ projections either side of attention
+
+def _bf16_value(bits) -> np.ndarray:
+    """BF16 bit patterns -> float64 values (the upper half of a binary32)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def _round_bf16(x) -> np.ndarray:
+    """float64 -> BF16 bits, round to nearest even (via the exact binary32 value when it is one;
+    the float64 is first rounded to binary32 to nearest, which cannot change the nearest-even
+    BF16 result unless it lands exactly on a BF16 midpoint: those cases are resolved on the
+    float64 value)."""
+    x = np.asarray(x, dtype=np.float64)
+    f = x.astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    lo = (u >> 16) << 16
+    hi = lo + (1 << 16)
+    vlo = lo.astype(np.uint32).view(np.float32).astype(np.float64)
+    vhi = hi.astype(np.uint32).view(np.float32).astype(np.float64)
+    # nearest of the two neighbours by the float64 value; exact ties to the even pattern
+    dlo, dhi = np.abs(x - vlo), np.abs(vhi - x)
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (((lo >> 16) & 1) == 1))
+    out = np.where(pick_hi, hi >> 16, lo >> 16).astype(np.uint16)
+    return out
+
+
+def project(x, w, x_is_f32: bool = False):
+    """Per-head projection Y[b, h, :] = X[b, h, :] W[h] (RAQ-MLA page, Figure 4: the query is
+    absorbed into the latent space through W_UK with A_c^-1 folded in, k_R is compensated on the
+    query side, and the latent readout leaves through W_UV with A_c^-1 folded in).
+    x: BF16 bits [B, H, K] (or float32 values when x_is_f32: they are first rounded to BF16,
+    the operand precision of the product); w: BF16 bits [H, K, N] or [K, N] (one matrix for
+    every head). Returns the exact products as float64 [B, H, N]."""
+    xv = _round_bf16_value(np.asarray(x, np.float32)) if x_is_f32 else _bf16_value(x)
+    wv = _bf16_value(w)
+    if wv.ndim == 2:
+        return np.einsum("bhk,kn->bhn", xv, wv)
+    return np.einsum("bhk,hkn->bhn", xv, wv)
+
+
+def _round_bf16_value(x32) -> np.ndarray:
+    return _bf16_value(_round_bf16(np.asarray(x32, np.float64)))
+
+
+def absorb_query(q_nope, w_uk, q_rope=None, r_comp=None):
+    """q_lat = BF16(q_nope W_UK[h]) [B, H, 512] and, with r_comp, q_rope' = BF16(q_rope r_comp)
+    [B, H, 64]: the decode's query inputs. Returns (q_lat bits, q_rope' bits or None, exact
+    q_lat float64, exact q_rope' float64 or None)."""
+    ql = project(q_nope, w_uk)
+    qr = project(q_rope, r_comp) if r_comp is not None else None
+    return _round_bf16(ql), (_round_bf16(qr) if qr is not None else None), ql, qr
+
+
+def up_project(o, w_uv):
+    """Y = BF16(O) W_UV[h] in float64: O float32 [B, H, 512] (the decode output), W_UV BF16
+    [H, 512, d_v]."""
+    return project(o, w_uv, x_is_f32=True)
