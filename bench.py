@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--sweep-batches", default="1,8,32")
     ap.add_argument("--sweep-heads", type=int, default=16)
     ap.add_argument("--sweep-max-tokens", type=int, default=1 << 20)
+    ap.add_argument("--proj", action="store_true",
+                    help="projections either side of attention: query absorption and W_UV up-projection")
     ap.add_argument("--transform", action="store_true",
                     help="per-layer cost of the latent transform A_c: standalone kernel vs fused in the writer")
     return ap.parse_args()
@@ -111,9 +113,11 @@ def peaks():
 
 
 def source_sha() -> str:
+    """Hash of the decode kernels' sources: the DRAM traffic recorded in a decode profile holds
+    only while these are unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_mla_kv_qcache_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in ("decode.cu", "decode_tc.cu", "ptx.cuh"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -506,6 +510,39 @@ SWEEP_BATCH_TOKENS = 1 << 23  # largest batch x context swept (bounds device mem
 FLUSH_BYTES = 512 * 1024 * 1024
 
 
+def flushed_call_us(fn, flush, stream, reps: int = 10, rounds: int = 5) -> float:
+    """Device time of one call that reads its inputs from HBM: a CUDA graph of `reps` x (512 MB
+    write that evicts L2, call) minus a graph of `reps` x (write), per call; median over
+    `rounds` replays of each (the graph launch itself is paid once per replay, not per call)."""
+    import torch
+    g_all, g_fl = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_all, stream=stream):
+        for k in range(reps):
+            flush.fill_(float(k))
+            fn()
+    with torch.cuda.graph(g_fl, stream=stream):
+        for k in range(reps):
+            flush.fill_(float(k))
+
+    def once(g):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3
+
+    with torch.cuda.stream(stream):
+        g_all.replay()
+        g_fl.replay()
+        torch.cuda.synchronize()
+        t_all, t_fl = [], []
+        for _ in range(rounds):  # interleaved, so both see the same clocks
+            t_all.append(once(g_all))
+            t_fl.append(once(g_fl))
+    return max(0.0, statistics.median(t_all) - statistics.median(t_fl)) / reps
+
+
 def bf16_decode_bytes(seq_lens, heads) -> int:
     """Bytes the unquantized decode must move: every token's BF16 row, queries and outputs."""
     B = len(seq_lens)
@@ -516,9 +553,10 @@ def run_sweep(args):
     """Decode latency of one layer over a C4R4 cache (page 128, sink 4, recent 128) and over an
     unquantized BF16 paged cache (page 64) holding the same tokens, for contexts of 1K..1M tokens
     and batches 1/8/32, as the normalised-latency tables of the low-bit MLA cache pages report:
-    delta = t_C4R4 / t_BF16 - 1. Both calls are captured as CUDA graphs; a 512 MB write before
-    every timed call evicts L2, so each call reads its cache from HBM (one decode of one layer,
-    whose cache the other layers' calls have evicted). Every sequence of a batch holds the same
+    delta = t_C4R4 / t_BF16 - 1. A 512 MB write before every call evicts L2, so each call reads
+    its cache from HBM (one decode of one layer, whose cache the other layers' calls have
+    evicted); per-call device time from CUDA graphs of (write, call) pairs minus graphs of the
+    writes alone. Every sequence of a batch holds the same
     synthetic rows (one seeded 1M-token draw; prefixes give the shorter contexts)."""
     import torch
 
@@ -588,29 +626,14 @@ def run_sweep(args):
                     q.mla_qcache_decode_attn_bf16(q_lat, q_rope, d_pt_b, P_b, lens, pool, wq.softmax_scale, out, lse,
                                                   ws_b, err)
 
-                graphs = []
                 with torch.cuda.stream(stream):
                     for fn in (call_q, call_b):
                         fn()
-                        torch.cuda.synchronize()
-                        g = torch.cuda.CUDAGraph()
-                        with torch.cuda.graph(g, stream=stream):
-                            fn()
-                        graphs.append(g)
-                    times = [[], []]
-                    for k in range(3 + iters):  # both sides alternate under the same clocks
-                        for side in (0, 1):
-                            flush.fill_(float(k))
-                            s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                            s_ev.record(stream)
-                            graphs[side].replay()
-                            e_ev.record(stream)
-                            if k >= 3:
-                                times[side].append((s_ev, e_ev))
                     torch.cuda.synchronize()
+                us = [flushed_call_us(call_q, flush, stream, reps=iters, rounds=5),
+                      flushed_call_us(call_b, flush, stream, reps=iters, rounds=5)]
                 if cache.error_bits() or int(err.item()):
                     raise RuntimeError("device error bits set during the sweep")
-                us = [statistics.median(a.elapsed_time(b) * 1e3 for a, b in ts) for ts in times]
                 seq = [T] * B
                 wb = workloads.Workload("sweep_c4r4", B, H, T, 4, 128)
                 bq, bb = decode_bytes(wb, seq, H), bf16_decode_bytes(seq, H)
@@ -620,13 +643,14 @@ def run_sweep(args):
                                "c4r4_hbm_frac": bq / (us[0] * 1e-6) / 1e9 / hbm_peak,
                                "bf16_hbm_frac": bb / (us[1] * 1e-6) / 1e9 / hbm_peak,
                                "c4r4_bytes": bq, "bf16_bytes": bb})
-                del graphs, cache, pool, ws_q, ws_b
+                del cache, pool, ws_q, ws_b
                 torch.cuda.empty_cache()
     print(json.dumps({
         "mode": "latency_sweep", "metric": "decode attention latency per layer, C4R4 vs BF16 paged; "
                                            "delta = t_C4R4 / t_BF16 - 1", "unit": "us", "heads": H,
         "cache": "C4R4 page 128 sink 4 recent 128", "comparator": "BF16 paged cache, page 64 (own kernel)",
-        "iters": iters, "statistic": "median", "l2": "512 MB write before every timed call",
+        "iters": iters, "statistic": "median of 5 graph replays of iters (flush, call) pairs minus flush-only "
+                                     "graphs, per call", "l2": "512 MB write before every timed call",
         "hbm_peak_gbs": hbm_peak, "peak_kind": peak_kind, "data": "synthetic", "points": points,
         "clocks": clk.summary()}))
     return 0
@@ -718,6 +742,61 @@ def run_transform(args):
     return 0
 
 
+# ------------------------------------------------------------------ projections either side of attention
+
+def run_proj(args):
+    """Query absorption (q_nope W_UK plus the 64 x 64 query-side k_R compensation) and the W_UV
+    up-projection of the attention output, per layer at decode batches 1..64, for 16 and 128
+    heads (d_nope = d_v = 128). A 512 MB write before every call evicts L2 (a layer's weights
+    come from HBM); per-call device time from CUDA graphs of (write, call) pairs minus graphs of
+    the writes alone. HBM fraction = (weights + inputs + outputs) / time / measured copy
+    bandwidth."""
+    import torch
+
+    import bit_mla_kv_qcache_gb300 as q
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    hbm_peak, _, peak_kind = peaks()
+    rng = np.random.default_rng(5)
+    iters = max(10, args.steps)
+    bf = lambda shape, scale: torch.from_numpy((rng.standard_normal(shape) * scale).astype(np.float32)).to(
+        torch.bfloat16).view(torch.int16).to(dev)
+    rows = []
+    with ClockSampler(0) as clk:
+        for H in (16, 128):
+            d = dv = 128
+            w_uk, w_uv, r_c = bf((H, d, 512), d ** -0.5), bf((H, 512, dv), 512 ** -0.5), bf((64, 64), 0.125)
+            for B in (1, 8, 32, 64):
+                qn, qr = bf((B, H, d), 1.0), bf((B, H, 64), 1.0)
+                ql = torch.empty((B, H, 512), dtype=torch.int16, device=dev)
+                qro = torch.empty((B, H, 64), dtype=torch.int16, device=dev)
+                o = torch.randn((B, H, 512), dtype=torch.float32, device=dev)
+                out = torch.empty((B, H, dv), dtype=torch.float32, device=dev)
+                ops = {"absorb": lambda: q.mla_qcache_absorb_query(qn, w_uk, ql, q_rope=qr, r_comp=r_c, q_rope_out=qro),
+                       "up_project": lambda: q.mla_qcache_up_project(o, w_uv, out)}
+                nbytes = {"absorb": w_uk.numel() * 2 + 8192 + B * H * (d + 64 + 512 + 64) * 2,
+                          "up_project": w_uv.numel() * 2 + B * H * (512 + dv) * 4}
+                res = {"heads": H, "batch": B}
+                with torch.cuda.stream(stream):
+                    for fn in ops.values():
+                        fn()
+                    torch.cuda.synchronize()
+                for name, fn in ops.items():
+                    us = flushed_call_us(fn, flush, stream, reps=iters)
+                    res[f"{name}_us"] = us
+                    res[f"{name}_hbm_frac"] = nbytes[name] / (us * 1e-6) / 1e9 / hbm_peak
+                rows.append(res)
+    print(json.dumps({"mode": "projections", "metric": "per-layer µs of the query absorption and the W_UV "
+                                                       "up-projection (d_nope = d_v = 128)",
+                      "unit": "us", "l2": "512 MB write before every timed call", "iters": iters,
+                      "statistic": "median of 5 graph replays, (flush, call) pairs minus flush-only, per call", "hbm_peak_gbs": hbm_peak, "peak_kind": peak_kind, "rows": rows,
+                      "clocks": clk.summary(), "data": "synthetic"}))
+    return 0
+
+
 def cpu_baseline(w):
     n_seq = max(1, w.batch // 16)
     step, scale = oracle_step_sample(w, n_seq)
@@ -738,6 +817,8 @@ def main():
         return run_sweep(args)
     if args.transform:
         return run_transform(args)
+    if args.proj:
+        return run_proj(args)
     return run_native(args, w)
 
 

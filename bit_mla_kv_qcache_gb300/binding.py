@@ -22,7 +22,8 @@ EXPORTS = ("mla_qcache_page_bytes", "mla_qcache_config_check", "mla_qcache_works
            "mla_qcache_write", "mla_qcache_decode_attn", "mla_qcache_strerror",
            "mla_qcache_decode_attn_noalloc", "mla_qcache_noalloc_scratch_bytes", "mla_qcache_advance",
            "mla_qcache_write_advance", "mla_qcache_decode_attn_bf16", "mla_qcache_bf16_workspace_bytes",
-           "mla_qcache_write_transformed", "mla_qcache_row_transform")
+           "mla_qcache_write_transformed", "mla_qcache_row_transform", "mla_qcache_absorb_query",
+           "mla_qcache_up_project")
 
 
 class Config(ctypes.Structure):
@@ -81,6 +82,10 @@ def lib() -> ctypes.CDLL:
                                                    i64, vp, vp, vp, vp]
         L.mla_qcache_row_transform.restype = ctypes.c_int
         L.mla_qcache_row_transform.argtypes = [i32, i32, vp, vp, vp, vp, vp]
+        L.mla_qcache_absorb_query.restype = ctypes.c_int
+        L.mla_qcache_absorb_query.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
+        L.mla_qcache_up_project.restype = ctypes.c_int
+        L.mla_qcache_up_project.argtypes = [i32, i32, i32, vp, vp, vp, vp]
         L.mla_qcache_bf16_workspace_bytes.restype = sz
         L.mla_qcache_bf16_workspace_bytes.argtypes = [i32, i32, i32, i32]
         L.mla_qcache_decode_attn_bf16.restype = ctypes.c_int
@@ -193,6 +198,31 @@ def mla_qcache_row_transform(x, a, out, err_word, stream=None) -> None:
     st = lib().mla_qcache_row_transform(n, d, _ptr(x, "x", 2), _ptr(a, "a", 2), _ptr(out, "out", 2),
                                         _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
     _raise(st, "mla_qcache_row_transform")
+
+
+def mla_qcache_absorb_query(q_nope, w_uk, q_lat, q_rope=None, r_comp=None, q_rope_out=None, stream=None) -> None:
+    """q_lat = q_nope W_UK[h] and, with r_comp, q_rope_out = q_rope r_comp (see include/mla_qcache.h)."""
+    B, H, d = q_nope.shape
+    if tuple(w_uk.shape) != (H, d, 512) or tuple(q_lat.shape) != (B, H, 512):
+        raise ValueError("absorb_query: q_nope [B, H, d], w_uk [H, d, 512], q_lat [B, H, 512]")
+    if r_comp is not None and (tuple(r_comp.shape) != (64, 64) or q_rope is None or q_rope_out is None):
+        raise ValueError("absorb_query: r_comp [64, 64] needs q_rope and q_rope_out [B, H, 64]")
+    st = lib().mla_qcache_absorb_query(
+        B, H, d, _ptr(q_nope, "q_nope", 2), _ptr(w_uk, "w_uk", 2), _ptr(q_rope, "q_rope", 2, allow_none=True),
+        _ptr(r_comp, "r_comp", 2, allow_none=True), _ptr(q_lat, "q_lat", 2),
+        _ptr(q_rope_out, "q_rope_out", 2, allow_none=True), _stream(stream))
+    _raise(st, "mla_qcache_absorb_query")
+
+
+def mla_qcache_up_project(o, w_uv, out, stream=None) -> None:
+    """out = BF16(O) W_UV[h] (float32 out, see include/mla_qcache.h)."""
+    B, H, _ = o.shape
+    d_v = w_uv.shape[2]
+    if tuple(w_uv.shape) != (H, 512, d_v) or tuple(out.shape) != (B, H, d_v):
+        raise ValueError("up_project: o [B, H, 512], w_uv [H, 512, d_v], out [B, H, d_v]")
+    st = lib().mla_qcache_up_project(B, H, d_v, _ptr(o, "o", dtype=torch.float32), _ptr(w_uv, "w_uv", 2),
+                                     _ptr(out, "out", dtype=torch.float32), _stream(stream))
+    _raise(st, "mla_qcache_up_project")
 
 
 def bf16_workspace_bytes(B: int, H: int, max_pages: int, page_size: int) -> int:

@@ -17,6 +17,7 @@ SOURCES = {  # file -> extra flags
     "writer.cu": ["-fmad=false"],  # exact rounding decisions: keep every product unfused
     "decode.cu": [],
     "decode_tc.cu": [],
+    "proj.cu": [],
 }
 
 

@@ -194,6 +194,42 @@ int mla_qcache_row_transform(int32_t n_rows, int32_t dim, const uint16_t* x, con
   return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
 }
 
+static int proj_checks(int32_t B, int32_t H, int32_t K, int32_t N, const void* x, const void* w, const void* y) {
+  if (B < 0 || B > (1 << 22) || H < 1 || H > 256 || K < 16 || K > mlaq::kProjMaxK || K % 16 || N < 32 || N % 32)
+    return MLA_QCACHE_ERR_SHAPE;
+  if (B > 0 && (!x || !w || !y)) return MLA_QCACHE_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16)) return MLA_QCACHE_ERR_ALIGN;
+  return MLA_QCACHE_OK;
+}
+
+int mla_qcache_absorb_query(int32_t B, int32_t H, int32_t d_nope, const uint16_t* q_nope, const uint16_t* w_uk,
+                            const uint16_t* q_rope, const uint16_t* r_comp, uint16_t* q_lat, uint16_t* q_rope_out,
+                            void* stream) {
+  int st = proj_checks(B, H, d_nope, mlaq::kLatent, q_nope, w_uk, q_lat);
+  if (st != MLA_QCACHE_OK) return st;
+  if ((r_comp == nullptr) != (q_rope_out == nullptr)) return MLA_QCACHE_ERR_NULL;
+  if (r_comp && (st = proj_checks(B, H, mlaq::kRope, mlaq::kRope, q_rope, r_comp, q_rope_out)) != MLA_QCACHE_OK)
+    return st;
+  if (B == 0) return MLA_QCACHE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  mlaq::ProjParams p{B, H, d_nope, mlaq::kLatent, q_nope, false, w_uk,
+                     static_cast<size_t>(d_nope) * mlaq::kLatent, q_lat, false};
+  const mlaq::ProjParams pr{B, H, mlaq::kRope, mlaq::kRope, q_rope, false, r_comp, 0, q_rope_out, false};
+  const cudaError_t e = mlaq::launch_proj(p, r_comp ? &pr : nullptr, s);  // one launch for both
+  return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
+}
+
+int mla_qcache_up_project(int32_t B, int32_t H, int32_t d_v, const float* o, const uint16_t* w_uv, float* out,
+                          void* stream) {
+  const int st = proj_checks(B, H, mlaq::kLatent, d_v, o, w_uv, out);
+  if (st != MLA_QCACHE_OK) return st;
+  if (B == 0) return MLA_QCACHE_OK;
+  const mlaq::ProjParams p{B, H, mlaq::kLatent, d_v, o, true, w_uv, static_cast<size_t>(mlaq::kLatent) * d_v, out,
+                           true};
+  const cudaError_t e = mlaq::launch_proj(p, nullptr, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
+}
+
 int mla_qcache_advance(const int32_t* cu_new, int32_t* seq_lens, int32_t B, void* stream) {
   if (!cu_new || !seq_lens) return MLA_QCACHE_ERR_NULL;
   if (B < 1) return MLA_QCACHE_ERR_SHAPE;

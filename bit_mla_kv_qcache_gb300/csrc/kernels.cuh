@@ -46,6 +46,21 @@ cudaError_t launch_write(const WriteParams& p, cudaStream_t stream);
 // out = x A row by row (BF16 rows of dim 64 or 512), the arithmetic of the transforming writer.
 cudaError_t launch_row_transform(int n_rows, int dim, const uint16_t* x, const uint16_t* a, uint16_t* out,
                                  int32_t* err, cudaStream_t stream);
+// Y[b, h, :] = X[b, h, :] W[h] for X [B][H][K] (BF16, or float32 rounded to BF16) and W
+// [H][K][N] BF16 (w_head_stride elements between heads, 0 = one matrix for every head);
+// Y [B][H][N] BF16 or float32. K % 16 == 0, 16 <= K <= kProjMaxK, N % 32 == 0.
+constexpr int kProjMaxK = 512;
+struct ProjParams {
+  int B, H, K, N;
+  const void* x;
+  bool x_f32;
+  const uint16_t* w;
+  size_t w_head_stride;
+  void* y;
+  bool y_f32;
+};
+// p1 (optional): a second product of the same B, H and operand types in the same launch.
+cudaError_t launch_proj(const ProjParams& p0, const ProjParams* p1, cudaStream_t stream);
 // seq_lens[b] += cu_new[b+1] - cu_new[b] for b in [0, B).
 cudaError_t launch_advance(const int32_t* cu_new, int32_t* seq_lens, int B, cudaStream_t stream);
 

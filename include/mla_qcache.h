@@ -265,6 +265,37 @@ int mla_qcache_row_transform(int32_t n_rows, int32_t dim, const uint16_t* x, con
                              int32_t* err_word, void* stream);
 
 /*
+ * Query absorption (RAQ-MLA page, Figure 4: the decode scores the latent directly, so the
+ * query's no-position part is carried into the latent space through W_UK, with A_c^-1 folded
+ * into W_UK offline; k_R's transform is compensated on the query side):
+ *   q_lat[b][h][:]      = BF16( q_nope[b][h][:] . w_uk[h] )        w_uk [H][d_nope][512]
+ *   q_rope_out[b][h][:] = BF16( q_rope[b][h][:] . r_comp )         r_comp [64][64], every head
+ * All BF16, row-major, 16-byte aligned; products on the tensor cores with float32 accumulation,
+ * each result rounded to BF16 to nearest-even (relative error within one BF16 rounding plus the
+ * float32 accumulation). r_comp and q_rope_out are both NULL (no compensation: pass q_rope to
+ * the decode unchanged) or both set. The outputs are the decode's q_lat / q_rope.
+ *   d_nope   a multiple of 16, 16..512 (128 for DeepSeek-V2-shaped layers). B 0..2^22, H 1..256.
+ * Errors: bad sizes -> MLA_QCACHE_ERR_SHAPE; NULL (with B > 0) -> MLA_QCACHE_ERR_NULL;
+ * misaligned -> MLA_QCACHE_ERR_ALIGN. Nothing is checked on the device.
+ */
+int mla_qcache_absorb_query(int32_t B, int32_t H, int32_t d_nope, const uint16_t* q_nope, const uint16_t* w_uk,
+                            const uint16_t* q_rope, const uint16_t* r_comp, uint16_t* q_lat, uint16_t* q_rope_out,
+                            void* stream);
+
+/*
+ * Up-projection of the decode output (RAQ-MLA page, Figure 4: the readout stays in the latent
+ * space and leaves through W_UV, with A_c^-1 folded into W_UV offline):
+ *   out[b][h][:] = BF16(o[b][h][:]) . w_uv[h]      o [B][H][512] float32 (mla_qcache_decode_attn's
+ *                                                  out), w_uv [H][512][d_v] BF16, out [B][H][d_v]
+ *                                                  float32
+ * The attention output enters the tensor cores rounded to BF16 (nearest-even), the sums are
+ * float32. d_v a multiple of 32 (128 for DeepSeek-V2-shaped layers); pointers 16-byte aligned.
+ * Errors: as mla_qcache_absorb_query.
+ */
+int mla_qcache_up_project(int32_t B, int32_t H, int32_t d_v, const float* o, const uint16_t* w_uv, float* out,
+                          void* stream);
+
+/*
  * Length update after a write (the pages leave the bookkeeping to the caller): for every
  * sequence b in [0, B), seq_lens[b] += cu_new[b+1] - cu_new[b], in one kernel on `stream`,
  * ordered after a preceding mla_qcache_write on the same stream. cu_new [B+1] and seq_lens [B]

@@ -139,6 +139,22 @@ def test_transform_entry_points_validate_on_the_host(L):
     assert lib.mla_qcache_row_transform(4, 512, p, p, ctypes.c_void_p(16 * 1024 + 2048), e, None) == -3  # overlaps x
 
 
+def test_projection_entry_points_validate_on_the_host(L):
+    lib = L.lib()
+    p, odd = ctypes.c_void_p(16 * 1024), ctypes.c_void_p(16 * 1024 + 8)
+    aq = lambda B, H, d, qr, r, qro, x=p: lib.mla_qcache_absorb_query(B, H, d, x, p, qr, r, p, qro, None)
+    assert aq(0, 16, 128, None, None, None) == 0  # nothing to do
+    assert aq(4, 16, 100, None, None, None) == -3 and aq(4, 16, 1024, None, None, None) == -3
+    assert aq(4, 0, 128, None, None, None) == -3
+    assert aq(4, 16, 128, p, p, None) == -1  # r_comp without an output
+    assert aq(4, 16, 128, None, p, p) == -1  # r_comp without q_rope
+    assert aq(4, 16, 128, None, None, None, x=odd) == -4
+    up = lambda B, H, dv, o=p: lib.mla_qcache_up_project(B, H, dv, o, p, p, None)
+    assert up(4, 16, 100) == -3 and up(4, 16, 0) == -3 and up(-1, 16, 128) == -3
+    assert up(4, 16, 128, o=None) == -1 and up(4, 16, 128, o=odd) == -4
+    assert up(0, 16, 128, o=None) == 0
+
+
 def test_product_path_has_no_cpu_fallback(L, monkeypatch):
     """Without the built library the binding raises instead of computing anything else."""
     import bit_mla_kv_qcache_gb300.binding as b
