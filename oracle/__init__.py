@@ -337,3 +337,43 @@ def up_project(o, w_uv):
     """Y = BF16(O) W_UV[h] in float64: O float32 [B, H, 512] (the decode output), W_UV BF16
     [H, 512, d_v]."""
     return project(o, w_uv, x_is_f32=True)
+
+
+# ------------------------------------------------------------------ multi-token decode
+
+def decode_multi(cfg: Config, q_lat, q_rope, q_len: int, page_table, seq_lens, pool, sink, ring,
+                 softmax_scale: float):
+    """Decode of q_len new tokens per sequence at once (a draft verified in one step, or a short
+    chunk): rows of q_lat [B, q_len * H, 512] / q_rope [B, q_len * H, 64] ordered [position i]
+    [head h]. The q_len tokens are the cache's last ones (written before the call); position i
+    sees the cache tokens t < T - (q_len - 1 - i), itself included, each with the values the
+    cache holds at length T (BF16 rows for t < S or t >= T - W, else the packed copy, as
+    token_values reads them). Softmax attention per row in float64, written out from the
+    definition. Returns (out float64 [B, q_len * H, 512], lse float64 [B, q_len * H])."""
+    q_lat = np.ascontiguousarray(q_lat, dtype=np.uint16)
+    q_rope = np.ascontiguousarray(q_rope, dtype=np.uint16)
+    B, R = q_lat.shape[0], q_lat.shape[1]
+    assert R % q_len == 0
+    H = R // q_len
+    scale = float(np.float32(softmax_scale))
+    out = np.zeros((B, R, LATENT), dtype=np.float64)
+    lse = np.full((B, R), -np.inf, dtype=np.float64)
+    for b in range(B):
+        T = int(seq_lens[b])
+        if T <= 0:
+            continue
+        V = np.stack([token_values(cfg, b, t, T, page_table, pool, sink, ring)[0] for t in range(T)])
+        ql = _bf16_value(q_lat[b])
+        qr = _bf16_value(q_rope[b])
+        for i in range(q_len):
+            T_i = T - (q_len - 1 - i)
+            if T_i <= 0:
+                continue
+            for h in range(H):
+                r = i * H + h
+                sc = scale * (V[:T_i, :LATENT] @ ql[r] + V[:T_i, LATENT:] @ qr[r])
+                m = sc.max()
+                w = np.exp(sc - m)
+                out[b, r] = (w @ V[:T_i, :LATENT]) / w.sum()
+                lse[b, r] = m + np.log(w.sum())
+    return out, lse
