@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--sweep-batches", default="1,8,32")
     ap.add_argument("--sweep-heads", type=int, default=16)
     ap.add_argument("--sweep-max-tokens", type=int, default=1 << 20)
+    ap.add_argument("--multi", action="store_true",
+                    help="multi-token decode: q_len new tokens per sequence in one call")
     ap.add_argument("--proj", action="store_true",
                     help="projections either side of attention: query absorption and W_UV up-projection")
     ap.add_argument("--transform", action="store_true",
@@ -742,6 +744,63 @@ def run_transform(args):
     return 0
 
 
+# ------------------------------------------------------------------ multi-token decode
+
+def run_multi(args):
+    """Decode of q_len = 1, 2, 4, 8 new tokens per sequence in one call over the headline cache
+    shape (C4R4, 16 heads, batch 32 at 8K tokens, and batch 1 at 128K); L2 flushed before every
+    call. At q_len * 16 a multiple of 64 the packed pages are read once for all positions."""
+    import torch
+
+    import bit_mla_kv_qcache_gb300 as q
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    hbm_peak, tensor_peak, peak_kind = peaks()
+    iters = max(10, args.steps)
+    rows = []
+    with ClockSampler(0) as clk:
+        for B, T in ((32, 8192), (1, 131072)):
+            w = workloads.Workload("multi_c4r4", B, 16, T, 4, 128)
+            inp = workloads.make_inputs(w, extra_pages=1)
+            to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else
+                                                np.ascontiguousarray(a)).to(dev)
+            cfg = q.make_config(**w.config_kwargs())
+            cache = q.QuantizedMLACache(cfg, B, inp.page_table.shape[1], inp.n_pages,
+                                        page_table=to_dev(inp.page_table), device=dev)
+            cache.write(to_dev(inp.c), to_dev(inp.kr), to_dev(inp.cu), T)
+            for q_len in (1, 2, 4, 8):
+                R = 16 * q_len
+                ql, qr = workloads.draw_queries(np.random.default_rng(q_len), B, R)
+                d_ql, d_qr = to_dev(ql), to_dev(qr)
+                out = torch.empty((B, R, 512), dtype=torch.float32, device=dev)
+                lse = torch.empty((B, R), dtype=torch.float32, device=dev)
+                ws = torch.empty(q.workspace_bytes(cfg, B, R, inp.page_table.shape[1]), dtype=torch.uint8, device=dev)
+                fn = lambda: q.mla_qcache_decode_attn_multi(cfg, q_len, d_ql, d_qr, cache.page_table, cache.seq_lens,
+                                                            cache.pool, cache.sink, cache.ring, w.softmax_scale, out,
+                                                            lse, ws, cache.err)
+                with torch.cuda.stream(stream):
+                    fn()
+                    torch.cuda.synchronize()
+                us = flushed_call_us(fn, flush, stream, reps=iters)
+                nbytes = decode_bytes(w, [T] * B, R)
+                rows.append({"batch": B, "T": T, "q_len": q_len, "rows": R, "us": us, "us_per_token": us / q_len,
+                             "hbm_frac": nbytes / (us * 1e-6) / 1e9 / hbm_peak,
+                             "tflops": decode_flops([T] * B, R) / (us * 1e-6) / 1e12})
+            if cache.error_bits():
+                raise RuntimeError("device error bits set in the multi-token benchmark")
+            del cache
+            torch.cuda.empty_cache()
+    print(json.dumps({"mode": "multi_token_decode", "metric": "decode µs per call for q_len new tokens per "
+                                                              "sequence (C4R4, 16 heads per position)",
+                      "unit": "us", "l2": "512 MB write before every timed call", "iters": iters,
+                      "hbm_peak_gbs": hbm_peak, "peak_kind": peak_kind, "rows": rows, "clocks": clk.summary(),
+                      "data": "synthetic"}))
+    return 0
+
+
 # ------------------------------------------------------------------ projections either side of attention
 
 def run_proj(args):
@@ -819,6 +878,8 @@ def main():
         return run_transform(args)
     if args.proj:
         return run_proj(args)
+    if args.multi:
+        return run_multi(args)
     return run_native(args, w)
 
 

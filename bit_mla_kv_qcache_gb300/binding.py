@@ -23,7 +23,7 @@ EXPORTS = ("mla_qcache_page_bytes", "mla_qcache_config_check", "mla_qcache_works
            "mla_qcache_decode_attn_noalloc", "mla_qcache_noalloc_scratch_bytes", "mla_qcache_advance",
            "mla_qcache_write_advance", "mla_qcache_decode_attn_bf16", "mla_qcache_bf16_workspace_bytes",
            "mla_qcache_write_transformed", "mla_qcache_row_transform", "mla_qcache_absorb_query",
-           "mla_qcache_up_project")
+           "mla_qcache_up_project", "mla_qcache_decode_attn_multi")
 
 
 class Config(ctypes.Structure):
@@ -82,6 +82,9 @@ def lib() -> ctypes.CDLL:
                                                    i64, vp, vp, vp, vp]
         L.mla_qcache_row_transform.restype = ctypes.c_int
         L.mla_qcache_row_transform.argtypes = [i32, i32, vp, vp, vp, vp, vp]
+        L.mla_qcache_decode_attn_multi.restype = ctypes.c_int
+        L.mla_qcache_decode_attn_multi.argtypes = [P(Config), i32, i32, i32, vp, vp, vp, i32, vp, vp, i64, vp, vp,
+                                                   ctypes.c_float, vp, vp, vp, sz, vp, vp]
         L.mla_qcache_absorb_query.restype = ctypes.c_int
         L.mla_qcache_absorb_query.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]
         L.mla_qcache_up_project.restype = ctypes.c_int
@@ -198,6 +201,24 @@ def mla_qcache_row_transform(x, a, out, err_word, stream=None) -> None:
     st = lib().mla_qcache_row_transform(n, d, _ptr(x, "x", 2), _ptr(a, "a", 2), _ptr(out, "out", 2),
                                         _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
     _raise(st, "mla_qcache_row_transform")
+
+
+def mla_qcache_decode_attn_multi(cfg: Config, q_len: int, q_lat, q_rope, page_table, seq_lens, pool, sink_buf,
+                                 recent_buf, softmax_scale: float, out, lse, workspace, err_word, stream=None) -> None:
+    """Decode of q_len new tokens per sequence (rows [B, q_len * H, ...] position-major; see
+    include/mla_qcache.h); workspace of workspace_bytes(cfg, B, q_len * H, max_pages)."""
+    B, R = q_lat.shape[0], q_lat.shape[1]
+    if R % q_len:
+        raise ValueError("q_lat rows must be q_len x heads")
+    st = lib().mla_qcache_decode_attn_multi(
+        ctypes.byref(cfg), B, R // q_len, int(q_len), _ptr(q_lat, "q_lat", 2), _ptr(q_rope, "q_rope", 2),
+        _ptr(page_table, "page_table", dtype=torch.int32), page_table.shape[1],
+        _ptr(seq_lens, "seq_lens", dtype=torch.int32), _ptr(pool, "pool", 1), pool.shape[0],
+        _ptr(sink_buf, "sink_buf", 2, allow_none=True) if cfg.n_sink else None, _ptr(recent_buf, "recent_buf", 2),
+        ctypes.c_float(softmax_scale), _ptr(out, "out", dtype=torch.float32), _ptr(lse, "lse", dtype=torch.float32),
+        _ptr(workspace, "workspace", 1), workspace.numel(), _ptr(err_word, "err_word", dtype=torch.int32),
+        _stream(stream))
+    _raise(st, "mla_qcache_decode_attn_multi")
 
 
 def mla_qcache_absorb_query(q_nope, w_uk, q_lat, q_rope=None, r_comp=None, q_rope_out=None, stream=None) -> None:

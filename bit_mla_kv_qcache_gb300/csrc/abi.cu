@@ -238,15 +238,19 @@ int mla_qcache_advance(const int32_t* cu_new, int32_t* seq_lens, int32_t B, void
   return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
 }
 
-int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H, const uint16_t* q_lat,
-                           const uint16_t* q_rope, const int32_t* page_table, int32_t max_pages,
-                           const int32_t* seq_lens, const uint8_t* pool, int64_t n_pages,
-                           const uint16_t* sink_buf, const uint16_t* recent_buf, float softmax_scale, float* out,
-                           float* lse, void* workspace, size_t workspace_bytes, int32_t* err_word, void* stream) {
+}  // extern "C"
+
+// H: rows per sequence (q_len positions x H / q_len heads, position-major).
+static int decode_impl(const mla_qcache_config* cfg, int32_t B, int32_t H, int32_t q_len, const uint16_t* q_lat,
+                       const uint16_t* q_rope, const int32_t* page_table, int32_t max_pages,
+                       const int32_t* seq_lens, const uint8_t* pool, int64_t n_pages, const uint16_t* sink_buf,
+                       const uint16_t* recent_buf, float softmax_scale, float* out, float* lse, void* workspace,
+                       size_t workspace_bytes, int32_t* err_word, void* stream) {
   int st = check_config(cfg);
   if (st != MLA_QCACHE_OK) return st;
   if (B < 1 || B > 65535 || H < 16 || H > 256 || H % 16 || max_pages < 1 || n_pages < 1)
     return MLA_QCACHE_ERR_SHAPE;
+  if (q_len < 1 || H % q_len || (H / q_len) % 16 || q_len - 1 > cfg->n_recent) return MLA_QCACHE_ERR_SHAPE;
   if (!q_lat || !q_rope || !page_table || !seq_lens || !pool || !recent_buf || !out || !lse || !workspace ||
       !err_word)
     return MLA_QCACHE_ERR_NULL;
@@ -291,8 +295,32 @@ int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H, c
   p.n_split = ns;
   p.n_q = nq;
   p.share_slots = mlaq::decode_share_slots(B, H, max_pages, cfg->page_size, ns, nq, sms);
+  p.q_len = q_len;
+  p.h_pos = H / q_len;
   const cudaError_t e = mlaq::launch_decode(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
+}
+
+extern "C" {
+
+int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H, const uint16_t* q_lat,
+                           const uint16_t* q_rope, const int32_t* page_table, int32_t max_pages,
+                           const int32_t* seq_lens, const uint8_t* pool, int64_t n_pages,
+                           const uint16_t* sink_buf, const uint16_t* recent_buf, float softmax_scale, float* out,
+                           float* lse, void* workspace, size_t workspace_bytes, int32_t* err_word, void* stream) {
+  return decode_impl(cfg, B, H, 1, q_lat, q_rope, page_table, max_pages, seq_lens, pool, n_pages, sink_buf,
+                     recent_buf, softmax_scale, out, lse, workspace, workspace_bytes, err_word, stream);
+}
+
+int mla_qcache_decode_attn_multi(const mla_qcache_config* cfg, int32_t B, int32_t H, int32_t q_len,
+                                 const uint16_t* q_lat, const uint16_t* q_rope, const int32_t* page_table,
+                                 int32_t max_pages, const int32_t* seq_lens, const uint8_t* pool, int64_t n_pages,
+                                 const uint16_t* sink_buf, const uint16_t* recent_buf, float softmax_scale,
+                                 float* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                 void* stream) {
+  if (q_len < 1 || H < 1 || static_cast<int64_t>(q_len) * H > 256) return MLA_QCACHE_ERR_SHAPE;
+  return decode_impl(cfg, B, q_len * H, q_len, q_lat, q_rope, page_table, max_pages, seq_lens, pool, n_pages,
+                     sink_buf, recent_buf, softmax_scale, out, lse, workspace, workspace_bytes, err_word, stream);
 }
 
 size_t mla_qcache_bf16_workspace_bytes(int32_t B, int32_t H, int32_t max_pages, int32_t page_size) {

@@ -244,10 +244,14 @@ template <bool kPaged>
 __device__ void bf16_split(const DecodeParams& p, const Shared& sh, int b, int T, int part,
                            const uint32_t (&qa)[8][4], const uint32_t (&qra)[4], State& st, int32_t& flags) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int s_end = kPaged ? 0 : min(p.S, T);
+  // Several new tokens per sequence: the CTA's rows belong to position i of the q_len tokens and
+  // see the prefix [0, T_vis), T_vis = T - (q_len - 1 - i); which copy a token is read from
+  // follows the cache length T (the recent window is [T - W, T)).
+  const int T_vis = (kPaged || p.q_len <= 1) ? T : T - (p.q_len - 1 - static_cast<int>(blockIdx.y) * 16 / p.h_pos);
+  const int s_end = kPaged ? 0 : max(0, min(p.S, T_vis));
   const int r_beg = kPaged ? 0 : max(T - p.W, s_end);
   const int has_sink = s_end > 0 ? 1 : 0;
-  const int n_all = has_sink + (T - r_beg + kTile - 1) / kTile;
+  const int n_all = has_sink + max(0, T_vis - r_beg + kTile - 1) / kTile;
   // this CTA's share of the sequence's protected tiles: [t_lo, t_lo + n_tiles)
   // (64-bit products only for the paged comparator, whose tables reach millions of tokens)
   const int t_lo = kPaged ? static_cast<int>((static_cast<long long>(n_all) * part) / p.n_q) : (n_all * part) / p.n_q;
@@ -276,7 +280,7 @@ __device__ void bf16_split(const DecodeParams& p, const Shared& sh, int b, int T
       count = s_end;
     } else {
       start = r_beg + (i - has_sink) * kTile;
-      count = min(kTile, T - start);
+      count = min(kTile, T_vis - start);
     }
   };
   auto row_ptr = [&](int t) -> const uint16_t* {

@@ -87,6 +87,8 @@ struct DecodeParams {
   int n_q;      // CTAs sharing the protected (BF16) tokens (partial slots n_split .. n_split+n_q-1)
   int share_slots;  // resident CTA slots of one wave left for packed shares (16-head kernel);
                     // > 0: balanced equal shares (more shares launched than one wave holds)
+  int q_len;        // new tokens decoded per sequence (rows [position][head]; 0 or 1: one)
+  int h_pos;        // rows per position (H / q_len), a multiple of 16
 };
 
 // Number of packed-token shares, and of CTAs for the protected tokens, of each (sequence,

@@ -188,6 +188,30 @@ int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows,
                      uint16_t* recent_buf, int32_t* err_word, void* stream);
 
 /*
+ * Decode of several new tokens per sequence in one call (a speculative draft verified in one
+ * step, or a short chunk): the q_len tokens are the cache's last ones, written before the
+ * call, and position i (0 <= i < q_len) attends to the cache tokens t < T - (q_len - 1 - i),
+ * itself included. Which copy a token is read from follows the cache length T as in
+ * mla_qcache_decode_attn (BF16 for t < S or t >= T - W, else the packed copy), so every
+ * position sees the same packed range and only the BF16 recent rows differ in their end; a
+ * position whose prefix is empty gets out = 0, lse = -inf. (The pages decode one token per
+ * step; this is the plainest extension: causal attention among the new tokens.)
+ *   H          heads per position, a multiple of 16; q_len * H <= 256; q_len - 1 <= W.
+ *   q_lat      [B][q_len][H][512] BF16, q_rope [B][q_len][H][64] BF16 (position-major rows);
+ *   out, lse   [B][q_len][H][512] float32, [B][q_len][H] float32.
+ *   workspace  mla_qcache_workspace_bytes(cfg, B, q_len * H, max_pages) bytes.
+ * Other arguments and errors as mla_qcache_decode_attn (with q_len * H rows); bad q_len ->
+ * MLA_QCACHE_ERR_SHAPE. q_len = 1 is mla_qcache_decode_attn. At q_len * H a multiple of 64 the
+ * packed pages are read once for all positions (64 rows per tensor-memory CTA).
+ */
+int mla_qcache_decode_attn_multi(const mla_qcache_config* cfg, int32_t B, int32_t H, int32_t q_len,
+                                 const uint16_t* q_lat, const uint16_t* q_rope, const int32_t* page_table,
+                                 int32_t max_pages, const int32_t* seq_lens, const uint8_t* pool, int64_t n_pages,
+                                 const uint16_t* sink_buf, const uint16_t* recent_buf, float softmax_scale,
+                                 float* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                 void* stream);
+
+/*
  * Unquantized comparator: the same single-token decode attention over a paged BF16 cache
  * (every token exact; the latency the quantized cache is measured against, QuantMLA page,
  * appendix Table 9 form: delta = t_quantized / t_BF16 - 1).

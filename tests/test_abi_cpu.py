@@ -155,6 +155,18 @@ def test_projection_entry_points_validate_on_the_host(L):
     assert up(0, 16, 128, o=None) == 0
 
 
+def test_multi_token_decode_validates_on_the_host(L):
+    lib = L.lib()
+    cfg = L.make_config(4, 128)  # W = 128
+    p = ctypes.c_void_p(16 * 1024)
+    f = ctypes.c_float(0.1)
+    mt = lambda H, ql: lib.mla_qcache_decode_attn_multi(ctypes.byref(cfg), 1, H, ql, p, p, p, 1, p, p, 1, p, p, f, p,
+                                                        p, p, 1 << 20, p, None)
+    assert mt(16, 0) == -3 and mt(24, 2) == -3  # q_len >= 1, heads a multiple of 16
+    assert mt(16, 17) == -3  # at most 256 rows
+    assert mt(1, 130) == -3  # q_len - 1 <= W (and heads a multiple of 16)
+
+
 def test_product_path_has_no_cpu_fallback(L, monkeypatch):
     """Without the built library the binding raises instead of computing anything else."""
     import bit_mla_kv_qcache_gb300.binding as b
