@@ -437,9 +437,10 @@ def e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream):
     """The step end to end through the public API: every step copies its new tokens and queries
     from pinned host memory to the device (one copy: staged contiguously, as a serving loop
     would), runs the fused write and the decode on the same rotated layer caches as the timed
-    steps, and copies O and LSE back to pinned host memory (one copy). Each layer's step (copy
-    in, write, decode, copy out) is captured once as a CUDA graph, as a serving loop drives a
-    decode step, and replayed."""
+    steps, and copies O and LSE back to pinned host memory (one copy). The copies run on their
+    own streams, double-buffered, so that step k+1's inputs arrive and step k's results leave
+    while step k+1 computes (the dependencies are explicit events); the whole timed sequence of
+    steps is captured once as a CUDA graph and replayed."""
     import torch
     B, H = w.batch, w.heads
     NL = len(caches)
@@ -448,62 +449,76 @@ def e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream):
     parts = [np.ascontiguousarray(a).view(np.int16).reshape(-1) for a in (c1, k1, inp.q_lat, inp.q_rope)]
     sizes = [x.size for x in parts]
     h_in = torch.from_numpy(np.concatenate(parts)).pin_memory()
-    d_in = torch.empty_like(h_in, device=dev)
     offs = np.cumsum([0] + sizes)
-    d_c = d_in[offs[0]:offs[1]].view(B, 512)
-    d_k = d_in[offs[1]:offs[2]].view(B, 64)
-    d_ql = d_in[offs[2]:offs[3]].view(B, H, 512)
-    d_qr = d_in[offs[3]:offs[4]].view(B, H, 64)
     n_out = B * H * 512
-    d_res = torch.empty(n_out + B * H, dtype=torch.float32, device=dev)  # O then LSE
-    out, lse = d_res[:n_out].view(B, H, 512), d_res[n_out:].view(B, H)
-    h_res = torch.empty_like(d_res, device="cpu").pin_memory()
+    d_in, d_res, h_res, views = [], [], [], []
+    for slot in range(2):
+        di = torch.empty_like(h_in, device=dev)
+        dr = torch.empty(n_out + B * H, dtype=torch.float32, device=dev)  # O then LSE
+        d_in.append(di)
+        d_res.append(dr)
+        h_res.append(torch.empty_like(dr, device="cpu").pin_memory())
+        views.append((di[offs[0]:offs[1]].view(B, 512), di[offs[1]:offs[2]].view(B, 64),
+                      di[offs[2]:offs[3]].view(B, H, 512), di[offs[3]:offs[4]].view(B, H, 64),
+                      dr[:n_out].view(B, H, 512), dr[n_out:].view(B, H)))
     cu1 = torch.arange(B + 1, dtype=torch.int32, device=dev)
     ws_buf = caches[0].workspace(H)
-
-    def step(cache, lens_in, lens_out):
-        d_in.copy_(h_in, non_blocking=True)
-        q.mla_qcache_write_advance(cfg, d_c, d_k, cu1, lens_in, lens_out, 1, cache.page_table, cache.pool,
-                                   cache.sink, cache.ring, cache.err)
-        q.mla_qcache_decode_attn(cfg, d_ql, d_qr, cache.page_table, lens_out, cache.pool, cache.sink, cache.ring,
-                                 w.softmax_scale, out, lse, ws_buf, cache.err)
-        h_res.copy_(d_res, non_blocking=True)
-
-    graphs = []
-    with torch.cuda.stream(stream):
-        for cache, alt in zip(caches, lens_alt):
-            pair = []
-            for lens_in, lens_out in ((cache.seq_lens, alt), (alt, cache.seq_lens)):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    step(cache, lens_in, lens_out)
-                pair.append(g)
-            graphs.append(pair)
-    torch.cuda.synchronize()
-    K = max(10, args.steps // 2)
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    # steps per graph: whole rounds over the layers, each layer an even number of times, so the
+    # two length arrays of every layer are back in their starting roles after each replay
+    K = 2 * NL * max(1, math.ceil(max(10, args.steps // 2) / (2 * NL)))
     k0 = sum(uses)
+    n_ev = K + 2
+    ev_h2d = [torch.cuda.Event() for _ in range(n_ev)]
+    ev_comp = [torch.cuda.Event() for _ in range(n_ev)]
+    ev_d2h = [torch.cuda.Event() for _ in range(n_ev)]
 
-    def replay(k):
-        layer = k % NL
-        graphs[layer][uses[layer] & 1].replay()
-        uses[layer] += 1
-
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for k in range(K):
+            slot = k & 1
+            layer = (k0 + k) % NL
+            cache, alt = caches[layer], lens_alt[layer]
+            lens_in, lens_out = (cache.seq_lens, alt) if uses[layer] % 2 == 0 else (alt, cache.seq_lens)
+            uses[layer] += 1
+            d_c, d_k, d_ql, d_qr, out, lse = views[slot]
+            with torch.cuda.stream(s_in):
+                if k >= 2:
+                    s_in.wait_event(ev_comp[k - 2])  # step k-2 no longer reads this input slot
+                d_in[slot].copy_(h_in, non_blocking=True)
+                ev_h2d[k].record(s_in)
+            stream.wait_event(ev_h2d[k])
+            if k >= 2:
+                stream.wait_event(ev_d2h[k - 2])  # step k-2's results have left this output slot
+            q.mla_qcache_write_advance(cfg, d_c, d_k, cu1, lens_in, lens_out, 1, cache.page_table, cache.pool,
+                                       cache.sink, cache.ring, cache.err, stream)
+            q.mla_qcache_decode_attn(cfg, d_ql, d_qr, cache.page_table, lens_out, cache.pool, cache.sink,
+                                     cache.ring, w.softmax_scale, out, lse, ws_buf, cache.err, stream)
+            ev_comp[k].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[k])
+                h_res[slot].copy_(d_res[slot], non_blocking=True)
+                ev_d2h[k].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+    torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        for k in range(3):
-            replay(k0 + k)
+        g.replay()  # warm-up replay
         torch.cuda.synchronize()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
-        for k in range(K):
-            replay(k0 + 3 + k)
+        g.replay()
         e.record(stream)
         torch.cuda.synchronize()
     us = s.elapsed_time(e) * 1e3 / K
     h2d = h_in.numel() * h_in.element_size()
-    d2h = h_res.numel() * h_res.element_size()
+    d2h = h_res[0].numel() * h_res[0].element_size()
     return {"value": us, "unit": "us/layer", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
-            "note": "public C ABI calls (fused write, decode) and one H2D + one D2H copy per step, captured per "
-                    "layer as CUDA graphs, layer caches rotated as in the timed steps"}
+            "note": "public C ABI calls (fused write, decode) with one H2D copy of the step's inputs and one "
+                    "D2H copy of O and LSE per step, copies on their own streams double-buffered against the "
+                    "compute, layer caches rotated as in the timed steps; the timed steps form one CUDA graph"}
 
 
 # ------------------------------------------------------------------ latency sweep against BF16
