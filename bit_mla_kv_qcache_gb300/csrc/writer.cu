@@ -166,21 +166,32 @@ __device__ __forceinline__ void xf_issue_latent(const CUtensorMap* map, int col0
   }
 }
 
+// OR of a predicate over the kXfCols threads (warps 0-1) that run the sums, on barrier 1 (the
+// other warps of the CTA are free meanwhile).
+__device__ __forceinline__ bool sum_warps_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred pi, po; setp.ne.u32 pi, %1, 0; barrier.cta.red.or.pred po, 1, %2, pi; selp.u32 %0, 1, 0, po; }"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(kXfCols)
+      : "memory");
+  return r != 0;
+}
+
+// Called by threads 0 .. kXfCols-1 only (thread 0 issued the boxes).
 __device__ bool latent_slice_transform(const float* s_x, const uint8_t* smem, uint64_t* bars, uint16_t& out) {
   float acc = 0.f;
   for (int rb = 0; rb < kXfBlocks; ++rb) {
     const bool ok = mbar_wait_bounded(bars + rb, 0, kXfWaitBudget);
-    if (__syncthreads_or(!ok)) {
+    if (sum_warps_or(!ok)) {
       if (threadIdx.x == 0)
         for (int j = rb; j < kXfBlocks; ++j) (void)mbar_wait_bounded(bars + j, 0, kXfWaitBudget >> 4);
       return false;
     }
-    if (threadIdx.x < kXfCols) {
-      const uint16_t* blk = reinterpret_cast<const uint16_t*>(smem + rb * kXfBoxBytes) + threadIdx.x;
-      const float* xb = s_x + rb * kXfBlockRows;
+    const uint16_t* blk = reinterpret_cast<const uint16_t*>(smem + rb * kXfBoxBytes) + threadIdx.x;
+    const float* xb = s_x + rb * kXfBlockRows;
 #pragma unroll 16
-      for (int i = 0; i < kXfBlockRows; ++i) acc = acc + xb[i] * bf16_bits_f32(blk[i * kXfCols]);
-    }
+    for (int i = 0; i < kXfBlockRows; ++i) acc = acc + xb[i] * bf16_bits_f32(blk[i * kXfCols]);
   }
   out = f32_bf16_bits(acc);
   return true;
@@ -220,12 +231,38 @@ __device__ __forceinline__ uint32_t transform_rope_pair(const uint16_t* x, const
   return static_cast<uint32_t>(f32_bf16_bits(a0)) | (static_cast<uint32_t>(f32_bf16_bits(a1)) << 16);
 }
 
+// Where row r goes: its sequence, that sequence's row offsets and length, and the id of the
+// page that receives it (loads only; the caller checks them). -1 where a load was not made.
+struct RowRef {
+  int b, r0, r1, s0;
+  int32_t pid;
+};
+__device__ __forceinline__ RowRef resolve_row(const WriteParams& p, int r) {
+  RowRef z{-1, 0, 0, -1, -1};
+  if (r < p.B) {
+    z.r0 = __ldg(p.cu_new + r);
+    z.r1 = __ldg(p.cu_new + r + 1);
+    if (z.r0 == r && z.r1 == r + 1) z.b = r;
+  }
+  if (z.b < 0) {
+    z.b = find_seq(p.cu_new, p.B, r);
+    z.r0 = __ldg(p.cu_new + z.b);
+    z.r1 = __ldg(p.cu_new + z.b + 1);
+  }
+  if (r < z.r0 || r >= z.r1 || z.r1 - z.r0 > p.max_new) return z;
+  z.s0 = __ldg(p.seq_lens + z.b);
+  if (z.s0 < 0) return z;
+  const int64_t pg = (static_cast<int64_t>(z.s0) + (r - z.r0)) / p.P;
+  if (pg < p.max_pages) z.pid = __ldg(p.page_table + static_cast<size_t>(z.b) * p.max_pages + pg);
+  return z;
+}
+
 // The cluster of token row r: CTA `rank` forms latent channels 64 rank .. 64 rank + 63 (one per
 // thread of its first two warps), CTA 1 also the 64 k_R channels; after the cluster barrier the
 // first CTA gathers the row in the per-token layout (thread: latent channels 4 tid .. 4 tid + 3;
 // warp-0 lanes: k_R channels 2 lane, 2 lane + 1). Every CTA of the cluster passes both barriers.
 __device__ void transform_token(const WriteParams& p, const CUtensorMap* a_map, int r, uint8_t* smem, uint2& cv,
-                                uint32_t& kr2) {
+                                uint32_t& kr2, RowRef& ref) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   const int rank = static_cast<int>(cl.block_rank());
@@ -233,6 +270,7 @@ __device__ void transform_token(const WriteParams& p, const CUtensorMap* a_map, 
   __shared__ float s_x[kRow];
   __shared__ __align__(16) uint16_t s_y[kXfCols + kRope];
   __shared__ __align__(8) uint64_t bars[kXfBars];
+  __shared__ RowRef s_ref;
   xf_bars_init(bars);
   const bool rope_here = rank == 1 && p.a_r != nullptr;
   if (p.a_c) xf_issue_latent(a_map, kXfCols * rank, smem, bars);
@@ -251,9 +289,13 @@ __device__ void transform_token(const WriteParams& p, const CUtensorMap* a_map, 
   }
   __syncthreads();
   bool ok = true;
-  uint16_t y = tid < kXfCols ? __ldg(c_row + kXfCols * rank + tid) : 0;
-  if (p.a_c) ok = latent_slice_transform(s_x, smem, bars, y);
-  if (tid < kXfCols) s_y[tid] = y;
+  if (tid < kXfCols) {  // warps 0-1: this CTA's 64 latent channels
+    uint16_t y = __ldg(c_row + kXfCols * rank + tid);
+    if (p.a_c) ok = latent_slice_transform(s_x, smem, bars, y);
+    s_y[tid] = y;
+  } else if (rank == 0 && tid == kXfCols) {  // meanwhile the first CTA finds where the row goes
+    s_ref = resolve_row(p, r);
+  }
   if (rank == 1 && tid < kRope) s_y[kXfCols + tid] = __ldg(k_row + tid);
   if (rope_here) {
     uint16_t yr = 0;
@@ -270,6 +312,7 @@ __device__ void transform_token(const WriteParams& p, const CUtensorMap* a_map, 
     const uint16_t* src = cl.map_shared_rank(s_y, (4 * tid) / kXfCols);
     cv = *reinterpret_cast<const uint2*>(src + ((4 * tid) & (kXfCols - 1)));
     if (warp == 0) kr2 = *reinterpret_cast<const uint32_t*>(cl.map_shared_rank(s_y, 1) + kXfCols + 2 * lane);
+    ref = s_ref;
   }
   cl.sync();  // the slices stay in place until the first CTA has read them
 }
@@ -278,28 +321,37 @@ __device__ void transform_token(const WriteParams& p, const CUtensorMap* a_map, 
 // 128 threads per new token: warp w owns latent group w (channels 128w..128w+127, four per
 // lane); lanes of warp 0 also carry the token's k_R (two channels each) for the retention copy.
 // kGiven: the row arrives in cv / kr2 (transformed by the token's cluster) instead of from c_new.
+// kGiven: the row arrives in cv / kr2 (transformed by the token's cluster) and where it goes in
+// ref, instead of from c_new and the offset, length and page-table loads.
 template <bool kGiven>
-__device__ void write_token(const WriteParams& p, int r, int (&s_cnt)[2][4], uint2 cv, uint32_t kr2) {
+__device__ void write_token(const WriteParams& p, int r, int (&s_cnt)[2][4], uint2 cv, uint32_t kr2,
+                            const RowRef& ref) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // decode steps write one row per sequence (cu_new[b] = b): then row r belongs to sequence r,
   // found with two independent loads instead of a dependent binary search
   int b = -1, r0 = 0, r1 = 0;
-  if (r < p.B) {
-    r0 = __ldg(p.cu_new + r);
-    r1 = __ldg(p.cu_new + r + 1);
-    if (r0 == r && r1 == r + 1) b = r;
-  }
-  if (b < 0) {
-    b = find_seq(p.cu_new, p.B, r);
-    r0 = __ldg(p.cu_new + b);
-    r1 = __ldg(p.cu_new + b + 1);
+  if constexpr (kGiven) {
+    b = ref.b;
+    r0 = ref.r0;
+    r1 = ref.r1;
+  } else {
+    if (r < p.B) {
+      r0 = __ldg(p.cu_new + r);
+      r1 = __ldg(p.cu_new + r + 1);
+      if (r0 == r && r1 == r + 1) b = r;
+    }
+    if (b < 0) {
+      b = find_seq(p.cu_new, p.B, r);
+      r0 = __ldg(p.cu_new + b);
+      r1 = __ldg(p.cu_new + b + 1);
+    }
   }
   if (r < r0 || r >= r1 || r1 - r0 > p.max_new) {  // inconsistent row offsets
     if (tid == 0) raise_err(p.err, kErrRows);
     return;
   }
   const int n_b = r1 - r0;
-  const int s0 = __ldg(p.seq_lens + b);
+  const int s0 = kGiven ? ref.s0 : __ldg(p.seq_lens + b);
   if (s0 < 0) {
     if (tid == 0) raise_err(p.err, kErrSeqOverflow);
     return;
@@ -331,7 +383,7 @@ __device__ void write_token(const WriteParams& p, int r, int (&s_cnt)[2][4], uin
     if (tid == 0) raise_err(p.err, kErrSeqOverflow);
     return;
   }
-  const int32_t pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
+  const int32_t pid = kGiven ? ref.pid : __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
   if (pid < 0 || pid >= p.n_pages) {
     if (tid == 0) raise_err(p.err, kErrBadPage);
     return;
@@ -567,11 +619,12 @@ __device__ __forceinline__ void write_body(const WriteParams& p, const CUtensorM
       const int r = blockIdx.x / kXfCtas;
       uint2 cv = make_uint2(0u, 0u);
       uint32_t kr2 = 0;
-      transform_token(p, a_map, r, reinterpret_cast<uint8_t*>(smem_f), cv, kr2);
+      RowRef ref{-1, 0, 0, -1, -1};
+      transform_token(p, a_map, r, reinterpret_cast<uint8_t*>(smem_f), cv, kr2, ref);
       if (blockIdx.x % kXfCtas != 0) return;  // the cluster's first CTA writes the token
-      write_token<true>(p, r, s_cnt, cv, kr2);
+      write_token<true>(p, r, s_cnt, cv, kr2, ref);
     } else {
-      write_token<false>(p, blockIdx.x, s_cnt, make_uint2(0u, 0u), 0u);
+      write_token<false>(p, blockIdx.x, s_cnt, make_uint2(0u, 0u), 0u, RowRef{-1, 0, 0, -1, -1});
     }
     return;
   }
@@ -607,8 +660,9 @@ __global__ void __launch_bounds__(128) row_transform_kernel(int dim, const uint1
   for (int i = threadIdx.x; i < dim; i += 128) s_x[i] = bf16_bits_f32(__ldg(x + r * dim + i));
   __syncthreads();
   uint16_t y = 0;
-  const bool ok = dim == kRope ? rope_transform(s_x, xf_smem, bars + kXfBlocks, threadIdx.x, y)
-                               : latent_slice_transform(s_x, xf_smem, bars, y);
+  bool ok = true;
+  if (dim == kRope) ok = rope_transform(s_x, xf_smem, bars + kXfBlocks, threadIdx.x, y);
+  else if (threadIdx.x < kXfCols) ok = latent_slice_transform(s_x, xf_smem, bars, y);
   if (!ok) {
     if (threadIdx.x == 0) raise_err(err, kErrTimeout);
     return;
