@@ -23,7 +23,7 @@ EXPORTS = ("mla_qcache_page_bytes", "mla_qcache_config_check", "mla_qcache_works
            "mla_qcache_decode_attn_noalloc", "mla_qcache_noalloc_scratch_bytes", "mla_qcache_advance",
            "mla_qcache_write_advance", "mla_qcache_decode_attn_bf16", "mla_qcache_bf16_workspace_bytes",
            "mla_qcache_write_transformed", "mla_qcache_row_transform", "mla_qcache_absorb_query",
-           "mla_qcache_up_project", "mla_qcache_decode_attn_multi")
+           "mla_qcache_up_project", "mla_qcache_decode_attn_multi", "mla_qcache_decode_plan")
 
 
 class Config(ctypes.Structure):
@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
                                                    i64, vp, vp, vp, vp]
         L.mla_qcache_row_transform.restype = ctypes.c_int
         L.mla_qcache_row_transform.argtypes = [i32, i32, vp, vp, vp, vp, vp]
+        L.mla_qcache_decode_plan.restype = ctypes.c_int
+        L.mla_qcache_decode_plan.argtypes = [P(Config), i32, i32, i32, i32, P(i32)]
         L.mla_qcache_decode_attn_multi.restype = ctypes.c_int
         L.mla_qcache_decode_attn_multi.argtypes = [P(Config), i32, i32, i32, vp, vp, vp, i32, vp, vp, i64, vp, vp,
                                                    ctypes.c_float, vp, vp, vp, sz, vp, vp]
@@ -201,6 +203,14 @@ def mla_qcache_row_transform(x, a, out, err_word, stream=None) -> None:
     st = lib().mla_qcache_row_transform(n, d, _ptr(x, "x", 2), _ptr(a, "a", 2), _ptr(out, "out", 2),
                                         _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
     _raise(st, "mla_qcache_row_transform")
+
+
+def decode_plan(cfg: Config, B: int, H: int, max_pages: int, num_sms: int) -> dict:
+    """The launch plan of a decode call (see include/mla_qcache.h); needs no GPU."""
+    out = (ctypes.c_int32 * 5)()
+    _raise(lib().mla_qcache_decode_plan(ctypes.byref(cfg), B, H, max_pages, num_sms, out), "mla_qcache_decode_plan")
+    return {"n_split": out[0], "n_protected": out[1], "share_slots": out[2], "tensor_memory": bool(out[3]),
+            "bf16_parts": out[4]}
 
 
 def mla_qcache_decode_attn_multi(cfg: Config, q_len: int, q_lat, q_rope, page_table, seq_lens, pool, sink_buf,

@@ -202,6 +202,22 @@ static int proj_checks(int32_t B, int32_t H, int32_t K, int32_t N, const void* x
   return MLA_QCACHE_OK;
 }
 
+int mla_qcache_decode_plan(const mla_qcache_config* cfg, int32_t B, int32_t H, int32_t max_pages, int32_t num_sms,
+                           int32_t* plan) {
+  const int st = check_config(cfg);
+  if (st != MLA_QCACHE_OK) return st;
+  if (!plan) return MLA_QCACHE_ERR_NULL;
+  if (B < 1 || H < 16 || H > 256 || H % 16 || max_pages < 1 || num_sms < 1) return MLA_QCACHE_ERR_SHAPE;
+  const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, num_sms);
+  const int nq = mlaq::decode_num_protected(B, H, max_pages, cfg->page_size, cfg->n_sink, cfg->n_recent, num_sms);
+  plan[0] = ns;
+  plan[1] = nq;
+  plan[2] = mlaq::decode_share_slots(B, H, max_pages, cfg->page_size, ns, nq, num_sms);
+  plan[3] = mlaq::decode_uses_tc(H) ? 1 : 0;
+  plan[4] = mlaq::decode_bf16_num_parts(B, H, max_pages, cfg->page_size, num_sms);
+  return MLA_QCACHE_OK;
+}
+
 int mla_qcache_absorb_query(int32_t B, int32_t H, int32_t d_nope, const uint16_t* q_nope, const uint16_t* w_uk,
                             const uint16_t* q_rope, const uint16_t* r_comp, uint16_t* q_lat, uint16_t* q_rope_out,
                             void* stream) {

@@ -289,6 +289,22 @@ int mla_qcache_row_transform(int32_t n_rows, int32_t dim, const uint16_t* x, con
                              int32_t* err_word, void* stream);
 
 /*
+ * The launch plan of a decode call for a problem size and an SM count (no GPU needed; what
+ * mla_qcache_decode_attn and mla_qcache_workspace_bytes use with the current device's count):
+ *   plan[0]  packed-token shares per (sequence, 16- or 64-head block)
+ *   plan[1]  CTAs sharing the BF16 (sink and recent) tokens per (sequence, 16-head block)
+ *   plan[2]  > 0: the balanced 16-head instance with this many CTA slots for packed shares
+ *            (more shares than one wave holds); 0: even slices of each sequence
+ *   plan[3]  1: the packed tokens run on the 64-head tensor-memory kernel (H % 64 == 0)
+ *   plan[4]  shares of the unquantized comparator (mla_qcache_decode_attn_bf16) at this
+ *            configuration's page size
+ * plan: host int32[5]. Errors: bad config -> MLA_QCACHE_ERR_CONFIG; NULL -> MLA_QCACHE_ERR_NULL;
+ * B < 1, H not a multiple of 16 in 16..256, max_pages < 1, num_sms < 1 -> MLA_QCACHE_ERR_SHAPE.
+ */
+int mla_qcache_decode_plan(const mla_qcache_config* cfg, int32_t B, int32_t H, int32_t max_pages, int32_t num_sms,
+                           int32_t* plan);
+
+/*
  * Query absorption (RAQ-MLA page, Figure 4: the decode scores the latent directly, so the
  * query's no-position part is carried into the latent space through W_UK, with A_c^-1 folded
  * into W_UK offline; k_R's transform is compensated on the query side):

@@ -177,3 +177,36 @@ def test_product_path_has_no_cpu_fallback(L, monkeypatch):
     src = open(os.path.join(ROOT, "bit_mla_kv_qcache_gb300", "binding.py")).read()
     src += open(os.path.join(ROOT, "bit_mla_kv_qcache_gb300", "cache.py")).read()
     assert "import oracle" not in src and "from oracle" not in src
+
+
+def test_decode_plan_shapes(L):
+    """The share rules of the decode, checked on the host for a 152-SM GB300 (three 16-head CTAs
+    or one 64-head CTA per SM)."""
+    sms, wave = 152, 3 * 152
+    c4 = L.make_config(4, 128)
+    # the 32 x 8K, 16-head configuration: one wave of 13 packed shares + 1 protected CTA
+    p = L.decode_plan(c4, 32, 16, 66, sms)
+    assert (p["n_split"], p["n_protected"], p["share_slots"], p["tensor_memory"]) == (13, 1, 0, False)
+    assert 32 * (p["n_split"] + p["n_protected"]) <= wave
+    # one sequence at 16 heads over a long table takes a whole wave of shares (not 64)
+    for mp in (514, 2050, 8194):
+        p = L.decode_plan(c4, 1, 16, mp, sms)
+        assert p["n_split"] == wave - 1 and p["share_slots"] == 0
+    # a short table: at least four 32-token tiles per share
+    p = L.decode_plan(c4, 1, 16, 10, sms)
+    assert p["n_split"] == 10 * 128 // 32 // 4
+    # eight long sequences: more shares than a wave, in the balanced instance
+    p = L.decode_plan(c4, 8, 16, 8194, sms)
+    assert p["n_split"] == 64 and p["share_slots"] == wave - 8 * p["n_protected"]
+    # 64-head blocks on the tensor-memory kernel: one wave of one CTA per SM
+    for B, H in ((1, 128), (8, 128), (2, 64)):
+        p = L.decode_plan(c4, B, H, 1026, sms)
+        assert p["tensor_memory"] and p["n_split"] == sms // (B * H // 64)
+    # the BF16 comparator: one wave of shares, or a whole number of waves when shares would be long
+    for B, mp in ((1, 8194), (8, 8194), (32, 2050)):
+        parts = L.decode_plan(c4, B, 16, mp, sms)["bf16_parts"]
+        per_wave = wave // B
+        assert parts <= 8 * per_wave and (parts <= per_wave or parts % per_wave == 0)
+    # errors
+    assert L.lib().mla_qcache_decode_plan(ctypes.byref(c4), 1, 24, 10, sms, (ctypes.c_int32 * 5)()) == -3
+    assert L.lib().mla_qcache_decode_plan(ctypes.byref(c4), 1, 16, 10, sms, None) == -1
