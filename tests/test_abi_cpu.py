@@ -210,3 +210,29 @@ def test_decode_plan_shapes(L):
     # errors
     assert L.lib().mla_qcache_decode_plan(ctypes.byref(c4), 1, 24, 10, sms, (ctypes.c_int32 * 5)()) == -3
     assert L.lib().mla_qcache_decode_plan(ctypes.byref(c4), 1, 16, 10, sms, None) == -1
+
+
+def test_binding_rejects_bad_shapes_before_any_call(L):
+    """Shape errors surface as ValueError in the binding (CPU tensors suffice: nothing is launched)."""
+    import torch
+    b = L
+    i16 = lambda *s: torch.zeros(*s, dtype=torch.int16)
+    f32 = lambda *s: torch.zeros(*s, dtype=torch.float32)
+    with pytest.raises(ValueError):
+        b.mla_qcache_absorb_query(i16(2, 16, 128), i16(16, 128, 256), i16(2, 16, 512))  # w_uk not [H, d, 512]
+    with pytest.raises(ValueError):
+        b.mla_qcache_absorb_query(i16(2, 16, 128), i16(16, 128, 512), i16(2, 16, 512), r_comp=i16(64, 64))
+    with pytest.raises(ValueError):
+        b.mla_qcache_up_project(f32(2, 16, 512), i16(16, 512, 128), f32(2, 16, 64))
+    with pytest.raises(ValueError):
+        b.mla_qcache_row_transform(i16(4, 512), i16(512, 64), i16(4, 512), torch.zeros(1, dtype=torch.int32))
+    cfg = b.make_config(4, 128)
+    with pytest.raises(ValueError):
+        b.mla_qcache_write_transformed(cfg, i16(1, 512), i16(1, 64), None, torch.zeros(1, dtype=torch.int32), 1,
+                                       None, None, None, None, None, a_c=i16(64, 64))
+    with pytest.raises(ValueError):
+        b.mla_qcache_decode_attn_multi(cfg, 3, i16(1, 16, 512), i16(1, 16, 64), None, None, None, None, None, 0.1,
+                                       None, None, None, None)
+    with pytest.raises(ValueError):
+        b.mla_qcache_decode_attn_bf16(i16(1, 16, 512), i16(1, 16, 64), None, 64, None, i16(4, 32, 576), 0.1,
+                                      None, None, None, None)
