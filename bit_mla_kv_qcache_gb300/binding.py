@@ -23,7 +23,8 @@ EXPORTS = ("mla_qcache_page_bytes", "mla_qcache_config_check", "mla_qcache_works
            "mla_qcache_decode_attn_noalloc", "mla_qcache_noalloc_scratch_bytes", "mla_qcache_advance",
            "mla_qcache_write_advance", "mla_qcache_decode_attn_bf16", "mla_qcache_bf16_workspace_bytes",
            "mla_qcache_write_transformed", "mla_qcache_row_transform", "mla_qcache_absorb_query",
-           "mla_qcache_up_project", "mla_qcache_decode_attn_multi", "mla_qcache_decode_plan")
+           "mla_qcache_up_project", "mla_qcache_decode_attn_multi", "mla_qcache_decode_plan",
+           "mla_qcache_selftest_wait_timeout")
 
 
 class Config(ctypes.Structure):
@@ -82,6 +83,8 @@ def lib() -> ctypes.CDLL:
                                                    i64, vp, vp, vp, vp]
         L.mla_qcache_row_transform.restype = ctypes.c_int
         L.mla_qcache_row_transform.argtypes = [i32, i32, vp, vp, vp, vp, vp]
+        L.mla_qcache_selftest_wait_timeout.restype = ctypes.c_int
+        L.mla_qcache_selftest_wait_timeout.argtypes = [vp, vp]
         L.mla_qcache_decode_plan.restype = ctypes.c_int
         L.mla_qcache_decode_plan.argtypes = [P(Config), i32, i32, i32, i32, P(i32)]
         L.mla_qcache_decode_attn_multi.restype = ctypes.c_int
@@ -203,6 +206,12 @@ def mla_qcache_row_transform(x, a, out, err_word, stream=None) -> None:
     st = lib().mla_qcache_row_transform(n, d, _ptr(x, "x", 2), _ptr(a, "a", 2), _ptr(out, "out", 2),
                                         _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
     _raise(st, "mla_qcache_row_transform")
+
+
+def selftest_wait_timeout(err_word, stream=None) -> None:
+    """Run the kernel whose bounded wait must give up (see include/mla_qcache.h)."""
+    _raise(lib().mla_qcache_selftest_wait_timeout(_ptr(err_word, "err_word", dtype=torch.int32), _stream(stream)),
+           "mla_qcache_selftest_wait_timeout")
 
 
 def decode_plan(cfg: Config, B: int, H: int, max_pages: int, num_sms: int) -> dict:

@@ -18,6 +18,7 @@ SOURCES = {  # file -> extra flags
     "decode.cu": [],
     "decode_tc.cu": [],
     "proj.cu": [],
+    "diag.cu": [],
 }
 
 

@@ -246,6 +246,13 @@ int mla_qcache_up_project(int32_t B, int32_t H, int32_t d_v, const float* o, con
   return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
 }
 
+int mla_qcache_selftest_wait_timeout(int32_t* err_word, void* stream) {
+  if (!err_word) return MLA_QCACHE_ERR_NULL;
+  if (!aligned(err_word, 4)) return MLA_QCACHE_ERR_ALIGN;
+  const cudaError_t e = mlaq::launch_wait_selftest(err_word, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
+}
+
 int mla_qcache_advance(const int32_t* cu_new, int32_t* seq_lens, int32_t B, void* stream) {
   if (!cu_new || !seq_lens) return MLA_QCACHE_ERR_NULL;
   if (B < 1) return MLA_QCACHE_ERR_SHAPE;

@@ -61,6 +61,8 @@ struct ProjParams {
 };
 // p1 (optional): a second product of the same B, H and operand types in the same launch.
 cudaError_t launch_proj(const ProjParams& p0, const ProjParams* p1, cudaStream_t stream);
+// A kernel whose bounded wait must give up: ORs kErrTimeout into *err.
+cudaError_t launch_wait_selftest(int32_t* err, cudaStream_t stream);
 // seq_lens[b] += cu_new[b+1] - cu_new[b] for b in [0, B).
 cudaError_t launch_advance(const int32_t* cu_new, int32_t* seq_lens, int B, cudaStream_t stream);
 

@@ -336,6 +336,15 @@ int mla_qcache_up_project(int32_t B, int32_t H, int32_t d_v, const float* o, con
                           void* stream);
 
 /*
+ * Self-test of the device-side failure detection: launches one kernel whose only wait can never
+ * complete (an mbarrier nothing arrives at), waited on with the bounded wait every kernel of
+ * this library uses. After ~1 ms the wait gives up, MLA_QCACHE_DEV_TIMEOUT is OR-ed into
+ * err_word (device int32, 4-byte aligned) and the kernel returns; the context stays usable.
+ * Errors: NULL -> MLA_QCACHE_ERR_NULL; misaligned -> MLA_QCACHE_ERR_ALIGN.
+ */
+int mla_qcache_selftest_wait_timeout(int32_t* err_word, void* stream);
+
+/*
  * Length update after a write (the pages leave the bookkeeping to the caller): for every
  * sequence b in [0, B), seq_lens[b] += cu_new[b+1] - cu_new[b], in one kernel on `stream`,
  * ordered after a preceding mla_qcache_write on the same stream. cu_new [B+1] and seq_lens [B]
