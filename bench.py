@@ -14,6 +14,7 @@ shards by sequence with no exchange); the time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -58,6 +59,11 @@ def parse():
                     help="multi-token decode: q_len new tokens per sequence in one call")
     ap.add_argument("--proj", action="store_true",
                     help="projections either side of attention: query absorption and W_UV up-projection")
+    ap.add_argument("--record-traffic", metavar="NCU_CSV",
+                    help="write profiles/traffic_<workload>.json from an ncu --csv log of dram__bytes_read.sum and "
+                         "dram__bytes_write.sum (no GPU needed)")
+    ap.add_argument("--traffic-kernel", default=None, help="kernel-name regex for --record-traffic")
+    ap.add_argument("--traffic-command", default="", help="the ncu command that wrote the log (recorded)")
     ap.add_argument("--transform", action="store_true",
                     help="per-layer cost of the latent transform A_c: standalone kernel vs fused in the writer")
     return ap.parse_args()
@@ -68,6 +74,20 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def replica_sequences(batch: int, rank: int, world: int) -> range:
+    """Global sequence ids owned by a rank of a replicas-only job: every rank serves its own
+    batch of sequences (weak scaling), rank r the ids [r*batch, (r+1)*batch)."""
+    if not 0 <= rank < world:
+        raise ValueError(f"rank {rank} outside a world of {world}")
+    return range(rank * batch, (rank + 1) * batch)
+
+
+def replica_workload(w: workloads.Workload, rank: int) -> workloads.Workload:
+    """The workload a rank serves: its own sequences, drawn from a seed of its own (rank 0
+    serves exactly the single-GPU workload)."""
+    return dataclasses.replace(w, seed=w.seed + 1000 * rank) if rank else w
 
 
 def max_over_ranks(value: float, device=None) -> float:
@@ -114,6 +134,11 @@ def peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def dominant_kernel_regex(w: workloads.Workload) -> str:
+    """Name pattern of the kernel that carries the decode's packed-page stream."""
+    return r"decode_tc_kernel" if w.heads % 64 == 0 else r"decode_kernel"
+
+
 def source_sha() -> str:
     """Hash of the decode kernels' sources: the DRAM traffic recorded in a decode profile holds
     only while these are unchanged."""
@@ -125,18 +150,64 @@ def source_sha() -> str:
     return h.hexdigest()[:16]
 
 
+def traffic_path(workload: str) -> str:
+    return os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+
+
 def profiled_traffic(workload: str):
-    """DRAM bytes per decode call from the committed ncu summary, if it was taken on the
-    current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+    """DRAM bytes (read + write) per launch of the dominant decode kernel, from the record that
+    ``--record-traffic`` wrote out of an ncu CSV, if it was taken on the current kernel sources
+    (else None)."""
+    path = traffic_path(workload)
     if not os.path.exists(path):
         return None
-    txt = open(path).read()
-    m_sha = re.search(r"source_sha:\s*([0-9a-f]+)", txt)
-    m_b = re.search(r"dram_bytes_per_call:\s*([0-9.e+]+)", txt)
-    if not m_sha or not m_b or m_sha.group(1) != source_sha():
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("source_sha") != source_sha():
         return None
-    return float(m_b.group(1))
+    return float(rec["dram_bytes_per_launch"])
+
+
+_BYTE_UNITS = {"byte": 1.0, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12,
+               "b": 1.0, "kb": 1e3, "mb": 1e6, "gb": 1e9, "kib": 1024.0, "mib": 1024.0 ** 2, "gib": 1024.0 ** 3}
+
+
+def ncu_dram_bytes(csv_path: str, kernel_regex: str):
+    """Per-launch dram__bytes_read.sum + dram__bytes_write.sum of the launches whose kernel name
+    matches kernel_regex, from an ncu ``--csv`` metrics log (one row per launch and metric)."""
+    import csv
+    rows = []
+    with open(csv_path, newline="") as f:
+        lines = [ln for ln in f if ln.startswith('"')]  # ncu's own log lines are not CSV rows
+    reader = csv.DictReader(lines)
+    per = {}
+    for r in reader:
+        name, metric = r.get("Kernel Name", ""), r.get("Metric Name", "")
+        if metric not in ("dram__bytes_read.sum", "dram__bytes_write.sum") or not re.search(kernel_regex, name):
+            continue
+        unit = r.get("Metric Unit", "byte").strip().lower()
+        val = float(r["Metric Value"].replace(",", "")) * _BYTE_UNITS[unit]
+        d = per.setdefault(r["ID"], {"kernel": name})
+        d[metric] = val
+    for launch_id, d in per.items():
+        if "dram__bytes_read.sum" in d and "dram__bytes_write.sum" in d:
+            rows.append((launch_id, d["kernel"], d["dram__bytes_read.sum"], d["dram__bytes_write.sum"]))
+    if not rows:
+        raise RuntimeError(f"no launch of a kernel matching {kernel_regex!r} with both DRAM metrics in {csv_path}")
+    return rows
+
+
+def record_traffic(csv_path: str, workload: str, kernel_regex: str, command: str) -> dict:
+    rows = ncu_dram_bytes(csv_path, kernel_regex)
+    per_launch = [rd + wr for _, _, rd, wr in rows]
+    rec = {"workload": workload, "kernel_regex": kernel_regex, "kernels": sorted({k for _, k, _, _ in rows}),
+           "launches": len(rows), "dram_bytes_read_per_launch": statistics.mean(r for _, _, r, _ in rows),
+           "dram_bytes_write_per_launch": statistics.mean(w for _, _, _, w in rows),
+           "dram_bytes_per_launch": statistics.mean(per_launch), "source_sha": source_sha(), "command": command}
+    with open(traffic_path(workload), "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    return rec
 
 
 # ------------------------------------------------------------------ clocks
@@ -199,59 +270,85 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle (baseline / reference arm)
 
-def oracle_step_sample(w: workloads.Workload, n_seq: int):
-    """Build an oracle cache for n_seq sequences; return a closure that times one sampled step
-    (write one token per sampled sequence + decode those sequences) and the scale factor to one
-    full step of the workload."""
+def oracle_step(w: workloads.Workload):
+    """Build the oracle's cache for the whole workload (every sequence, prefilled by the oracle
+    writer) and return a closure that runs one full layer step on it: the oracle writes one new
+    token to every sequence, then decodes every sequence and head. Nothing is sampled or scaled:
+    the closure's time is the time of one step of the workload."""
     import oracle
-    n_seq = max(1, min(n_seq, w.batch))
-    lens = workloads.seq_lens_for(w)[:n_seq]
-    inp = workloads.make_inputs(w, seq_lens=lens, extra_pages=1)
+    inp = workloads.make_inputs(w, extra_pages=1)
+    B = w.batch
     cfg = oracle.make_config(**w.config_kwargs())
     pool = np.zeros((inp.n_pages, oracle.page_bytes(cfg)), np.uint8)
-    sink = np.zeros((n_seq, cfg.n_sink, 576), np.uint16)
-    ring = np.zeros((n_seq, cfg.n_recent, 576), np.uint16)
-    oracle.write(cfg, inp.c, inp.kr, inp.cu, np.zeros(n_seq, np.int32), int(lens.max()), inp.page_table, pool, sink,
-                 ring)
+    sink = np.zeros((B, cfg.n_sink, 576), np.uint16)
+    ring = np.zeros((B, cfg.n_recent, 576), np.uint16)
+    oracle.write(cfg, inp.c, inp.kr, inp.cu, np.zeros(B, np.int32), int(inp.seq_lens.max()), inp.page_table, pool,
+                 sink, ring)
     rng = np.random.default_rng(123)
-    state = {"lens": lens.astype(np.int32).copy()}
+    state = {"lens": inp.seq_lens.astype(np.int32).copy()}
+    max_tokens = inp.page_table.shape[1] * w.page_size
 
     def step():
-        c1, k1 = workloads.draw_tokens(rng, n_seq, w.latent_dist, inp.outliers, w.outlier_scale)
+        c1, k1 = workloads.draw_tokens(rng, B, w.latent_dist, inp.outliers, w.outlier_scale)
+        if int(state["lens"].max()) + 1 > max_tokens:  # keep within the page table: restart from the prefill
+            state["lens"] = inp.seq_lens.astype(np.int32).copy()
         t0 = time.perf_counter()
-        oracle.write(cfg, c1, k1, np.arange(n_seq + 1, dtype=np.int32), state["lens"], 1, inp.page_table, pool, sink,
+        oracle.write(cfg, c1, k1, np.arange(B + 1, dtype=np.int32), state["lens"], 1, inp.page_table, pool, sink,
                      ring)
         state["lens"] = state["lens"] + 1
         oracle.decode(cfg, inp.q_lat, inp.q_rope, inp.page_table, state["lens"], pool, sink, ring, w.softmax_scale)
         return time.perf_counter() - t0
 
-    return step, w.batch / n_seq
+    return step
 
 
 def cpu_cores() -> int:
-    if os.environ.get("OMP_NUM_THREADS"):
-        return int(os.environ["OMP_NUM_THREADS"])
     return os.cpu_count() or 1
+
+
+def oracle_threads_summary(step, all_threads: int, steps_all: int, steps_1: int):
+    """Time the oracle step at all threads (steps_all steps) and at one thread (steps_1 steps)
+    on the same work; returns (us per step at all threads, summary dict)."""
+    import oracle
+    oracle.set_threads(all_threads)
+    t_all = [step() for _ in range(steps_all)]
+    oracle.set_threads(1)
+    t_1 = [step() for _ in range(steps_1)]
+    oracle.set_threads(all_threads)
+    us_all = statistics.mean(t_all) * 1e6
+    us_1 = statistics.mean(t_1) * 1e6
+    return us_all, {"threads_all": {"value": us_all, "unit": "us/layer", "threads": all_threads, "steps": steps_all},
+                    "threads_1": {"value": us_1, "unit": "us/layer", "threads": 1, "steps": steps_1}}
 
 
 def run_reference(args, w):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    n_seq = max(1, w.batch // 16)
-    step, scale = oracle_step_sample(w, n_seq)
+    import oracle
+    cores = cpu_cores()
+    oracle.set_threads(cores)
+    step = oracle_step(w)
     for _ in range(max(0, min(args.warmup, 1))):
         step()
+    t0 = time.perf_counter()
     times = [step() for _ in range(args.steps)]
-    us = statistics.mean(times) * scale * 1e6
+    wall = time.perf_counter() - t0
+    us = statistics.mean(times) * 1e6
+    oracle.set_threads(1)
+    t1 = step() * 1e6
+    oracle.set_threads(cores)
+    sample = (f"the whole workload, unscaled: per step the oracle writes one token to each of the {w.batch} "
+              f"sequences and decodes all {w.batch} x {w.heads} heads over every cached token")
     line = {
         "impl": "reference", "metric": METRIC, "value": us, "unit": "us/layer", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(w, 0),
-        "cpu_baseline": {"value": us, "unit": "us/layer", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": f"oracle write of 1 token + decode for {n_seq} of {w.batch} sequences per step, "
-                                   f"scaled x{scale:g} to the full batch"},
+        "timed_wall_s": wall,
+        "cpu_baseline": {"value": us, "unit": "us/layer", "cores": cores, "kind": "oracle", "sample": sample,
+                         "threads_all": {"value": us, "unit": "us/layer", "threads": cores, "steps": args.steps},
+                         "threads_1": {"value": t1, "unit": "us/layer", "threads": 1, "steps": 1}},
         "e2e": {"value": us, "unit": "us/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -278,6 +375,7 @@ def run_native(args, w):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    w = replica_workload(w, rank)
     cfg = q.make_config(**w.config_kwargs())
     B, H = w.batch, w.heads
 
@@ -872,19 +970,27 @@ def run_proj(args):
 
 
 def cpu_baseline(w):
-    n_seq = max(1, w.batch // 16)
-    step, scale = oracle_step_sample(w, n_seq)
-    step()
-    times = [step() for _ in range(3)]
-    us = statistics.mean(times) * scale * 1e6
-    return {"value": us, "unit": "us/layer", "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"oracle write of 1 token + decode for {n_seq} of {w.batch} sequences, 3 steps, "
-                      f"scaled x{scale:g} to the full batch"}
+    """The oracle on the host cores, one full unscaled step of the workload at all threads and
+    one at a single thread (the same work)."""
+    import oracle
+    cores = cpu_cores()
+    oracle.set_threads(cores)
+    step = oracle_step(w)
+    step()  # warm-up
+    us_all, d = oracle_threads_summary(step, cores, 1, 1)
+    return {"value": us_all, "unit": "us/layer", "cores": cores, "kind": "oracle",
+            "sample": f"the whole workload, unscaled: one step (one token written to each of the {w.batch} "
+                      f"sequences, then the decode of all {w.batch} x {w.heads} heads over every cached token)",
+            **d}
 
 
 def main():
     args = parse()
     w = workloads.WORKLOADS[args.workload]
+    if args.record_traffic:
+        regex = args.traffic_kernel or dominant_kernel_regex(w)
+        print(json.dumps(record_traffic(args.record_traffic, w.name, regex, args.traffic_command)))
+        return 0
     if args.impl == "reference":
         return run_reference(args, w)
     if args.sweep:

@@ -140,6 +140,27 @@ def _ptr(t, name, elem_size=None, dtype=None, allow_none=False):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _check_decode_shapes(q_lat, q_rope, page_table, seq_lens, out, lse, rows_per_seq=None):
+    """Shapes every decode entry point relies on, checked before any library call: a mis-shaped
+    output, length or page table would otherwise become an out-of-bounds device access."""
+    if q_lat is None or q_lat.dim() != 3 or q_lat.shape[2] != 512:
+        raise ValueError(f"q_lat must be [B, H, 512], got {None if q_lat is None else tuple(q_lat.shape)}")
+    B, R = q_lat.shape[0], q_lat.shape[1]
+    if rows_per_seq is not None and R != rows_per_seq:
+        raise ValueError(f"q_lat must have {rows_per_seq} rows per sequence, got {R}")
+    if q_rope is None or tuple(q_rope.shape) != (B, R, 64):
+        raise ValueError(f"q_rope must be [{B}, {R}, 64], got {None if q_rope is None else tuple(q_rope.shape)}")
+    if out is None or tuple(out.shape) != (B, R, 512):
+        raise ValueError(f"out must be [{B}, {R}, 512], got {None if out is None else tuple(out.shape)}")
+    if lse is None or tuple(lse.shape) != (B, R):
+        raise ValueError(f"lse must be [{B}, {R}], got {None if lse is None else tuple(lse.shape)}")
+    if seq_lens is None or seq_lens.dim() != 1 or seq_lens.shape[0] != B:
+        raise ValueError(f"seq_lens must be [{B}], got {None if seq_lens is None else tuple(seq_lens.shape)}")
+    if page_table is None or page_table.dim() != 2 or page_table.shape[0] != B:
+        raise ValueError(f"page_table must be [{B}, max_pages], got "
+                         f"{None if page_table is None else tuple(page_table.shape)}")
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -226,9 +247,10 @@ def mla_qcache_decode_attn_multi(cfg: Config, q_len: int, q_lat, q_rope, page_ta
                                  recent_buf, softmax_scale: float, out, lse, workspace, err_word, stream=None) -> None:
     """Decode of q_len new tokens per sequence (rows [B, q_len * H, ...] position-major; see
     include/mla_qcache.h); workspace of workspace_bytes(cfg, B, q_len * H, max_pages)."""
-    B, R = q_lat.shape[0], q_lat.shape[1]
-    if R % q_len:
+    if q_len < 1 or q_lat is None or q_lat.dim() != 3 or q_lat.shape[1] % q_len:
         raise ValueError("q_lat rows must be q_len x heads")
+    _check_decode_shapes(q_lat, q_rope, page_table, seq_lens, out, lse)
+    B, R = q_lat.shape[0], q_lat.shape[1]
     st = lib().mla_qcache_decode_attn_multi(
         ctypes.byref(cfg), B, R // q_len, int(q_len), _ptr(q_lat, "q_lat", 2), _ptr(q_rope, "q_rope", 2),
         _ptr(page_table, "page_table", dtype=torch.int32), page_table.shape[1],
@@ -273,9 +295,10 @@ def mla_qcache_decode_attn_bf16(q_lat, q_rope, page_table, page_size: int, seq_l
                                 out, lse, workspace, err_word, stream=None) -> None:
     """Decode attention over a paged BF16 cache kv_pool [n_pages, page_size, 576] (the
     unquantized comparator, see include/mla_qcache.h)."""
-    B, H = q_lat.shape[0], q_lat.shape[1]
     if kv_pool.dim() != 3 or kv_pool.shape[1] != page_size or kv_pool.shape[2] != 576:
         raise ValueError(f"kv_pool must be [n_pages, {page_size}, 576], got {tuple(kv_pool.shape)}")
+    _check_decode_shapes(q_lat, q_rope, page_table, seq_lens, out, lse)
+    B, H = q_lat.shape[0], q_lat.shape[1]
     st = lib().mla_qcache_decode_attn_bf16(
         B, H, _ptr(q_lat, "q_lat", 2), _ptr(q_rope, "q_rope", 2), _ptr(page_table, "page_table", dtype=torch.int32),
         page_table.shape[1], int(page_size), _ptr(seq_lens, "seq_lens", dtype=torch.int32),
@@ -295,6 +318,7 @@ def mla_qcache_advance(cu_new, seq_lens, stream=None) -> None:
 def mla_qcache_decode_attn(cfg: Config, q_lat, q_rope, page_table, seq_lens, pool, sink_buf, recent_buf,
                            softmax_scale: float, out, lse, workspace, err_word, stream=None) -> None:
     """Decode attention over the quantized cache (see include/mla_qcache.h)."""
+    _check_decode_shapes(q_lat, q_rope, page_table, seq_lens, out, lse)
     B, H = q_lat.shape[0], q_lat.shape[1]
     st = lib().mla_qcache_decode_attn(
         ctypes.byref(cfg), B, H, _ptr(q_lat, "q_lat", 2), _ptr(q_rope, "q_rope", 2),
@@ -316,6 +340,7 @@ def mla_qcache_decode_attn_noalloc(cfg: Config, q_lat, q_rope, page_table, seq_l
                                    softmax_scale: float, out, lse, err_word, stream=None) -> None:
     """Decode attention without a workspace argument: for callers that cannot allocate device
     memory, it runs on a scratch buffer compiled into the library (see include/mla_qcache.h)."""
+    _check_decode_shapes(q_lat, q_rope, page_table, seq_lens, out, lse)
     B, H = q_lat.shape[0], q_lat.shape[1]
     st = lib().mla_qcache_decode_attn_noalloc(
         ctypes.byref(cfg), B, H, _ptr(q_lat, "q_lat", 2), _ptr(q_rope, "q_rope", 2),

@@ -28,6 +28,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -1334,19 +1336,21 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 // Device address of the scratch for the current device. The host-side name of the array is only
 // a stand-in, so the address is looked up once per device (with that device current) and cached.
+// The cache slots are atomics: host threads whose first calls on a device overlap may each look
+// the address up, and every one of them stores the same value.
 cudaError_t noalloc_scratch(void** out) {
-  static void* addr[64] = {};
+  static std::atomic<void*> addr[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  void* a = addr[dev].load(std::memory_order_acquire);
+  if (a == nullptr) {
+    e = cudaGetSymbolAddress(&a, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    addr[dev] = p;
+    addr[dev].store(a, std::memory_order_release);
   }
-  *out = addr[dev];
+  *out = a;
   return cudaSuccess;
 }
 

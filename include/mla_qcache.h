@@ -403,7 +403,10 @@ int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H,
  * cudaFree or allocating library routine.
  *
  * The first call on a device looks up the scratch's device address (cudaGetSymbolAddress, with
- * that device current) and caches it; make that first call before any stream capture. Every
+ * that device current) and caches it; make that first call before any stream capture. Host
+ * threads may make their first calls concurrently (the cache is atomic). cudaDeviceReset
+ * reloads the library's device code, after which the cached address is stale: a process that
+ * resets a device must not call this entry point on it again. Every
  * call shares the one array and leaves its contents behind; nothing in it needs to start at
  * zero because each call writes every partial result it later reads. Calls that overlap on the
  * GPU (two streams, or two host threads) race on the scratch: serialize them.

@@ -105,10 +105,25 @@ def lib():
         _lib.oracle_decode_bf16.argtypes = [ctypes.c_int, ctypes.c_int, P(u16), P(u16), P(i32), ctypes.c_int,
                                             ctypes.c_int, P(i32), P(u16), ctypes.c_int64, ctypes.c_float, P(d),
                                             P(d)]
+        _lib.oracle_set_threads.restype = None
+        _lib.oracle_set_threads.argtypes = [ctypes.c_int]
+        _lib.oracle_max_threads.restype = ctypes.c_int
+        _lib.oracle_max_threads.argtypes = []
         _lib.oracle_row_transform.restype = None
         _lib.oracle_row_transform.argtypes = [ctypes.c_int, ctypes.c_int, P(u16), P(u16), P(ctypes.c_float),
                                               P(u16)]
     return _lib
+
+
+def set_threads(n: int) -> int:
+    """Threads of the oracle's parallel loops (timing only; results do not depend on it).
+    Returns the count now in effect."""
+    lib().oracle_set_threads(int(n))
+    return int(lib().oracle_max_threads())
+
+
+def max_threads() -> int:
+    return int(lib().oracle_max_threads())
 
 
 def _ptr(a: np.ndarray, ctype):

@@ -27,6 +27,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define LATENT 512
 #define ROPE 64
@@ -594,4 +597,21 @@ void oracle_row_transform(int n_rows, int dim, const uint16_t* x, const uint16_t
       out[(size_t)r * dim + j] = f32_to_bf16_rne(acc);
     }
   }
+}
+
+/* Threads of the parallel loops over heads (timing of the oracle only: every head's result is
+ * computed by one thread in the same order whatever the count). */
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+  omp_set_num_threads(n > 0 ? n : 1);
+#else
+  (void)n;
+#endif
+}
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
 }

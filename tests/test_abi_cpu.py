@@ -236,3 +236,21 @@ def test_binding_rejects_bad_shapes_before_any_call(L):
     with pytest.raises(ValueError):
         b.mla_qcache_decode_attn_bf16(i16(1, 16, 512), i16(1, 16, 64), None, 64, None, i16(4, 32, 576), 0.1,
                                       None, None, None, None)
+    from bit_mla_kv_qcache_gb300 import binding
+    # the single-token decode wrappers (workspace and allocation-free): every tensor's shape is
+    # checked against q_lat's [B, H] before a pointer is taken
+    B, H = 2, 16
+    good = dict(q_lat=i16(B, H, 512), q_rope=i16(B, H, 64), page_table=torch.zeros((B, 4), dtype=torch.int32),
+                seq_lens=torch.zeros(B, dtype=torch.int32), out=f32(B, H, 512), lse=f32(B, H))
+    bad = [("q_lat", i16(B, H, 256)), ("q_rope", i16(B, H, 32)), ("q_rope", i16(B + 1, H, 64)),
+           ("out", f32(B, H, 256)), ("out", f32(B, H - 1, 512)), ("lse", f32(B)), ("lse", f32(B, H + 16)),
+           ("seq_lens", torch.zeros(B + 1, dtype=torch.int32)), ("page_table", torch.zeros((B + 1, 4), dtype=torch.int32)),
+           ("page_table", torch.zeros(4, dtype=torch.int32))]
+    for name, t in bad:
+        a = dict(good, **{name: t})
+        with pytest.raises(ValueError):
+            b.mla_qcache_decode_attn(cfg, a["q_lat"], a["q_rope"], a["page_table"], a["seq_lens"], None, None, None,
+                                     0.1, a["out"], a["lse"], None, None)
+        with pytest.raises(ValueError):
+            binding.mla_qcache_decode_attn_noalloc(cfg, a["q_lat"], a["q_rope"], a["page_table"], a["seq_lens"], None, None,
+                                             None, 0.1, a["out"], a["lse"], None)

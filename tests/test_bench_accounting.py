@@ -31,3 +31,24 @@ def test_c2r4_and_short_sequences():
 def test_bf16_bytes_and_flops():
     assert bench.bf16_decode_bytes([1000, 24], 16) == 1024 * 1152 + 2 * 16 * 1152 + 2 * 16 * 513 * 4
     assert bench.decode_flops([1000, 24], 64) == 1024 * 64 * 2 * (576 + 512)
+
+
+def test_traffic_record_from_ncu_csv(tmp_path, monkeypatch):
+    """roofline.traffic comes from a JSON written by --record-traffic out of ncu's CSV (units
+    converted, read + write per launch of the matching kernel, other kernels ignored)."""
+    import bench
+    csv = tmp_path / "t.csv"
+    head = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size",'
+            '"Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"\n')
+    row = lambda i, k, m, u, v: f'"{i}","1","python","h","{k}","1","7","(128, 1, 1)","(32, 1, 14)","0","10.3","s","{m}","{u}","{v}"\n'
+    dk = "void mlaq::decode_kernel<4, false, false>(mlaq::DecodeParams)"
+    ck = "void mlaq::combine_kernel(mlaq::DecodeParams)"
+    csv.write_text("==PROF== Connected\n" + head + row(0, dk, "dram__bytes_read.sum", "Mbyte", "84.85") +
+                   row(0, dk, "dram__bytes_write.sum", "Kbyte", "3,110") + row(1, ck, "dram__bytes_read.sum", "Mbyte", "14.7") +
+                   row(1, ck, "dram__bytes_write.sum", "byte", "1000") + row(2, dk, "dram__bytes_read.sum", "Gbyte", "0.08485") +
+                   row(2, dk, "dram__bytes_write.sum", "byte", "3110000"))
+    monkeypatch.setattr(bench, "traffic_path", lambda w: str(tmp_path / f"traffic_{w}.json"))
+    rec = bench.record_traffic(str(csv), "v2lite_c4r4_b32_h16_t8k", r"decode_kernel", "ncu ...")
+    assert rec["launches"] == 2
+    assert abs(rec["dram_bytes_per_launch"] - 87.96e6) < 1.0
+    assert bench.profiled_traffic("v2lite_c4r4_b32_h16_t8k") == rec["dram_bytes_per_launch"]
