@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra-workloads", default="auto",
+                    help="other workloads measured in the same run ('auto': the target configurations when the "
+                         "default workload runs; 'none'; or a comma-separated list)")
     ap.add_argument("--sweep", action="store_true",
                     help="latency sweep: C4R4 decode against the BF16 paged comparator over 1K..1M tokens")
     ap.add_argument("--sweep-batches", default="1,8,32")
@@ -364,6 +367,10 @@ def config_dict(w, layers):
 
 # ------------------------------------------------------------------ GPU arm
 
+EXTRA_WORKLOADS = ("v2lite_c4r4_b32_h16_t32k", "ragged_c2r4_b64_h16_serve", "wide_c2r4_b8_h128_t32k",
+                   "long_c4r4_b1_h128_t128k")
+
+
 def run_native(args, w):
     import torch
 
@@ -375,15 +382,42 @@ def run_native(args, w):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = replica_workload(w, rank)
+    result = measure_workload(args, replica_workload(w, rank), q, dev, args.steps, args.warmup, args.layers,
+                              with_e2e=not args.no_e2e)
+    extras = [] if args.extra_workloads == "none" else (
+        list(EXTRA_WORKLOADS) if args.extra_workloads == "auto" and w.name == DEFAULT_WORKLOAD else
+        [x for x in args.extra_workloads.split(",") if x and x != "auto"])
+    if extras:
+        result["workloads"] = {}
+        for name in extras:
+            we = replica_workload(workloads.WORKLOADS[name], rank)
+            r = measure_workload(args, we, q, dev, min(args.steps, 10), 3, 0, with_e2e=False)
+            result["workloads"][name] = {k: r[k] for k in ("value", "unit", "steps", "decode_us", "write_and_advance_us",
+                                                             "packed_cache_gbs", "decode_tflops", "roofline",
+                                                             "gpu_launches", "clocks", "config")}
+            torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(result))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def measure_workload(args, w, q, dev, steps, warmup, layers, with_e2e):
+    """The timed steps of one workload: layer caches built by the writer, K write+decode steps
+    replayed from CUDA graphs over rotated caches, then a decode-only pass for the roofline."""
+    import torch
+    ws, rank, local = dist_env()
     cfg = q.make_config(**w.config_kwargs())
     B, H = w.batch, w.heads
 
-    steps_total = args.warmup + args.steps + 8
+    steps_total = warmup + steps + 8
     inp = workloads.make_inputs(w, extra_pages=math.ceil(steps_total / w.page_size) + 1)
     max_pages = inp.page_table.shape[1]
     per_layer = inp.n_pages * q.page_bytes(cfg)
-    NL = args.layers or max(2, math.ceil(3 * L2_BYTES / per_layer) + 1)
+    NL = layers or max(2, math.ceil(3 * L2_BYTES / per_layer) + 1)
 
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else
                                    np.ascontiguousarray(a)).to(dev)
@@ -422,9 +456,19 @@ def run_native(args, w):
         q.mla_qcache_decode_attn(cfg, q_lat, q_rope, cache.page_table, lens, cache.pool, cache.sink,
                                  cache.ring, w.softmax_scale, out, lse, ws_buf, cache.err)
 
+    def pending_step(cache, lens_in):
+        q.mla_qcache_decode_attn_pending(cfg, q_lat, q_rope, cache.page_table, lens_in, c_new, kr_new, cu1, 1,
+                                         cache.pool, cache.sink, cache.ring, w.softmax_scale, out, lse, ws_buf,
+                                         cache.err)
+
+    write_stream = torch.cuda.Stream(device=dev)
+
     # Two CUDA graphs per layer (write + decode, lengths A -> B and B -> A) replayed alternately:
-    # the timed region replays exactly K of them. A second live pass replays decode-only graphs
-    # with CUDA events around each call to measure the decode kernels for the roofline.
+    # the timed region replays exactly K of them. Inside a step the writer (with the length
+    # update) runs on a forked stream concurrently with the decode of the pending rows, joined
+    # before the step ends (the next step's decode reads what this step wrote). A second live
+    # pass replays decode-only graphs with CUDA events around each call to measure the decode
+    # kernels for the roofline.
     g_step, g_dec = [], []
     with torch.cuda.stream(stream):
         for cache in caches:  # warm the code paths once before capture
@@ -435,8 +479,11 @@ def run_native(args, w):
             for lens_in, lens_out in ((cache.seq_lens, alt), (alt, cache.seq_lens)):
                 gs = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(gs, stream=stream):
-                    write_step(cache, lens_in, lens_out)
-                    decode_step(cache, lens_out)
+                    write_stream.wait_stream(stream)
+                    with torch.cuda.stream(write_stream):
+                        write_step(cache, lens_in, lens_out)
+                    pending_step(cache, lens_in)
+                    stream.wait_stream(write_stream)
                 pair.append(gs)
             gd = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gd, stream=stream):
@@ -454,7 +501,7 @@ def run_native(args, w):
     head_start = torch.empty(int(1.5e9) // 4, dtype=torch.float32, device=dev)  # lets the host queue ahead
 
     with torch.cuda.stream(stream):
-        for k in range(args.warmup):
+        for k in range(warmup):
             replay_step(k)
         torch.cuda.synchronize()
         if ws > 1:
@@ -463,15 +510,15 @@ def run_native(args, w):
         with ClockSampler(local) as clk:
             head_start.fill_(1.0)
             start.record(stream)
-            for k in range(args.steps):
-                replay_step(args.warmup + k)
+            for k in range(steps):
+                replay_step(warmup + k)
             end.record(stream)
             torch.cuda.synchronize()
         total_ms = start.elapsed_time(end)
         # decode-only pass (same caches, lengths unchanged): per-call device time
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         head_start.fill_(2.0)
-        for k in range(args.steps):
+        for k in range(steps):
             ev[k][0].record(stream)
             g_dec[k % NL].replay()
             ev[k][1].record(stream)
@@ -482,7 +529,7 @@ def run_native(args, w):
     if any(c.error_bits() for c in caches):
         raise RuntimeError("device error bits set during the timed region")
 
-    us_step = total_ms * 1e3 / args.steps
+    us_step = total_ms * 1e3 / steps
     dec_us = statistics.mean(dec_ms) * 1e3
     # sequence lengths seen by the decode-only pass (after the timed steps)
     mean_T = np.maximum(caches[0].seq_lens.cpu().numpy(), lens_alt[0].cpu().numpy())  # the newer of the two
@@ -509,26 +556,21 @@ def run_native(args, w):
         launches_per_step = 3  # fused write + length update, decode, merge
 
     result = {
-        "metric": METRIC, "value": us_step * 1.0, "unit": "us/layer", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": us_step / 1e3, "higher_is_better": False, "scaling": "weak",
+        "metric": METRIC, "value": us_step * 1.0, "unit": "us/layer", "n_gpus": ws, "steps": steps,
+        "warmup": warmup, "ms_per_step": us_step / 1e3, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(w, NL),
         "decode_us": dec_us, "write_and_advance_us": max(0.0, us_step - dec_us),
         "packed_cache_gbs": achieved, "fraction_of_8tbs": achieved / 8000.0,
         "decode_tflops": tflops,
         "roofline": roofline,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step * steps,
         "clocks": clk.summary(),
     }
 
-    if not args.no_e2e:
+    if with_e2e:
         result["e2e"] = e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream)
-    if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w)
-    if rank == 0:
-        print(json.dumps(result))
-    if ws > 1:
-        torch.distributed.destroy_process_group()
-    return 0
+    del caches, g_step, g_dec, head_start
+    return result
 
 
 def e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream):
@@ -561,7 +603,7 @@ def e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream):
                       dr[:n_out].view(B, H, 512), dr[n_out:].view(B, H)))
     cu1 = torch.arange(B + 1, dtype=torch.int32, device=dev)
     ws_buf = caches[0].workspace(H)
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    s_in, s_out, s_wr = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     # steps per graph: whole rounds over the layers, each layer an even number of times, so the
     # two length arrays of every layer are back in their starting roles after each replay
     K = 2 * NL * max(1, math.ceil(max(10, args.steps // 2) / (2 * NL)))
@@ -590,10 +632,13 @@ def e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream):
             stream.wait_event(ev_h2d[k])
             if k >= 2:
                 stream.wait_event(ev_d2h[k - 2])  # step k-2's results have left this output slot
+            s_wr.wait_stream(stream)  # the write forks off after the step's inputs arrived
             q.mla_qcache_write_advance(cfg, d_c, d_k, cu1, lens_in, lens_out, 1, cache.page_table, cache.pool,
-                                       cache.sink, cache.ring, cache.err, stream)
-            q.mla_qcache_decode_attn(cfg, d_ql, d_qr, cache.page_table, lens_out, cache.pool, cache.sink,
-                                     cache.ring, w.softmax_scale, out, lse, ws_buf, cache.err, stream)
+                                       cache.sink, cache.ring, cache.err, s_wr)
+            q.mla_qcache_decode_attn_pending(cfg, d_ql, d_qr, cache.page_table, lens_in, d_c, d_k, cu1, 1, cache.pool,
+                                             cache.sink, cache.ring, w.softmax_scale, out, lse, ws_buf, cache.err,
+                                             stream)
+            stream.wait_stream(s_wr)  # joined: the next step reads what this write stored
             ev_comp[k].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_comp[k])
@@ -601,6 +646,7 @@ def e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream):
                 ev_d2h[k].record(s_out)
         stream.wait_stream(s_in)
         stream.wait_stream(s_out)
+        stream.wait_stream(s_wr)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         g.replay()  # warm-up replay
@@ -614,9 +660,10 @@ def e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream):
     h2d = h_in.numel() * h_in.element_size()
     d2h = h_res[0].numel() * h_res[0].element_size()
     return {"value": us, "unit": "us/layer", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
-            "note": "public C ABI calls (fused write, decode) with one H2D copy of the step's inputs and one "
-                    "D2H copy of O and LSE per step, copies on their own streams double-buffered against the "
-                    "compute, layer caches rotated as in the timed steps; the timed steps form one CUDA graph"}
+            "note": "public C ABI calls (fused write with the length update on a forked stream, concurrent with "
+                    "the decode of the pending rows) with one H2D copy of the step's inputs and one D2H copy of O "
+                    "and LSE per step, copies on their own streams double-buffered against the compute, layer "
+                    "caches rotated as in the timed steps; the timed steps form one CUDA graph"}
 
 
 # ------------------------------------------------------------------ latency sweep against BF16

@@ -24,7 +24,7 @@ EXPORTS = ("mla_qcache_page_bytes", "mla_qcache_config_check", "mla_qcache_works
            "mla_qcache_write_advance", "mla_qcache_decode_attn_bf16", "mla_qcache_bf16_workspace_bytes",
            "mla_qcache_write_transformed", "mla_qcache_row_transform", "mla_qcache_absorb_query",
            "mla_qcache_up_project", "mla_qcache_decode_attn_multi", "mla_qcache_decode_plan",
-           "mla_qcache_selftest_wait_timeout")
+           "mla_qcache_selftest_wait_timeout", "mla_qcache_decode_attn_pending")
 
 
 class Config(ctypes.Structure):
@@ -87,6 +87,9 @@ def lib() -> ctypes.CDLL:
         L.mla_qcache_selftest_wait_timeout.argtypes = [vp, vp]
         L.mla_qcache_decode_plan.restype = ctypes.c_int
         L.mla_qcache_decode_plan.argtypes = [P(Config), i32, i32, i32, i32, P(i32)]
+        L.mla_qcache_decode_attn_pending.restype = ctypes.c_int
+        L.mla_qcache_decode_attn_pending.argtypes = [P(Config), i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, i32, vp, i64,
+                                                     vp, vp, ctypes.c_float, vp, vp, vp, sz, vp, vp]
         L.mla_qcache_decode_attn_multi.restype = ctypes.c_int
         L.mla_qcache_decode_attn_multi.argtypes = [P(Config), i32, i32, i32, vp, vp, vp, i32, vp, vp, i64, vp, vp,
                                                    ctypes.c_float, vp, vp, vp, sz, vp, vp]
@@ -329,6 +332,31 @@ def mla_qcache_decode_attn(cfg: Config, q_lat, q_rope, page_table, seq_lens, poo
         _ptr(workspace, "workspace", 1), workspace.numel() * workspace.element_size(),
         _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
     _raise(st, "mla_qcache_decode_attn")
+
+
+def mla_qcache_decode_attn_pending(cfg: Config, q_lat, q_rope, page_table, seq_lens, c_new, kr_new, cu_new,
+                                   max_new: int, pool, sink_buf, recent_buf, softmax_scale: float, out, lse, workspace,
+                                   err_word, stream=None) -> None:
+    """Decode of the cache as the pending write of rows c_new / kr_new / cu_new will leave it
+    (seq_lens: lengths before that write); the write may run concurrently on another stream
+    (see include/mla_qcache.h)."""
+    _check_decode_shapes(q_lat, q_rope, page_table, seq_lens, out, lse)
+    B, H = q_lat.shape[0], q_lat.shape[1]
+    if cu_new is None or cu_new.dim() != 1 or cu_new.shape[0] != B + 1:
+        raise ValueError(f"cu_new must be [{B + 1}]")
+    if c_new is None or c_new.dim() != 2 or c_new.shape[1] != 512 or kr_new is None or \
+            tuple(kr_new.shape) != (c_new.shape[0], 64):
+        raise ValueError("c_new must be [rows, 512] and kr_new [rows, 64]")
+    st = lib().mla_qcache_decode_attn_pending(
+        ctypes.byref(cfg), B, H, _ptr(q_lat, "q_lat", 2), _ptr(q_rope, "q_rope", 2),
+        _ptr(page_table, "page_table", dtype=torch.int32), page_table.shape[1],
+        _ptr(seq_lens, "seq_lens", dtype=torch.int32), _ptr(c_new, "c_new", 2), _ptr(kr_new, "kr_new", 2),
+        _ptr(cu_new, "cu_new", dtype=torch.int32), int(max_new), _ptr(pool, "pool", 1), pool.shape[0],
+        _ptr(sink_buf, "sink_buf", 2, allow_none=True) if cfg.n_sink else None, _ptr(recent_buf, "recent_buf", 2),
+        ctypes.c_float(softmax_scale), _ptr(out, "out", dtype=torch.float32), _ptr(lse, "lse", dtype=torch.float32),
+        _ptr(workspace, "workspace", 1), workspace.numel() * workspace.element_size(),
+        _ptr(err_word, "err_word", dtype=torch.int32), _stream(stream))
+    _raise(st, "mla_qcache_decode_attn_pending")
 
 
 def noalloc_scratch_bytes() -> int:

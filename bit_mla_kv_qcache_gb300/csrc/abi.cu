@@ -264,11 +264,19 @@ int mla_qcache_advance(const int32_t* cu_new, int32_t* seq_lens, int32_t B, void
 }  // extern "C"
 
 // H: rows per sequence (q_len positions x H / q_len heads, position-major).
+// Rows of a write that has not run yet (mla_qcache_decode_attn_pending); cu_new == nullptr: none.
+struct PendingRows {
+  const uint16_t* c_new = nullptr;
+  const uint16_t* kr_new = nullptr;
+  const int32_t* cu_new = nullptr;
+  int32_t max_new = 0;
+};
+
 static int decode_impl(const mla_qcache_config* cfg, int32_t B, int32_t H, int32_t q_len, const uint16_t* q_lat,
                        const uint16_t* q_rope, const int32_t* page_table, int32_t max_pages,
                        const int32_t* seq_lens, const uint8_t* pool, int64_t n_pages, const uint16_t* sink_buf,
                        const uint16_t* recent_buf, float softmax_scale, float* out, float* lse, void* workspace,
-                       size_t workspace_bytes, int32_t* err_word, void* stream) {
+                       size_t workspace_bytes, int32_t* err_word, void* stream, const PendingRows& pend = PendingRows()) {
   int st = check_config(cfg);
   if (st != MLA_QCACHE_OK) return st;
   if (B < 1 || B > 65535 || H < 16 || H > 256 || H % 16 || max_pages < 1 || n_pages < 1)
@@ -320,6 +328,10 @@ static int decode_impl(const mla_qcache_config* cfg, int32_t B, int32_t H, int32
   p.share_slots = mlaq::decode_share_slots(B, H, max_pages, cfg->page_size, ns, nq, sms);
   p.q_len = q_len;
   p.h_pos = H / q_len;
+  p.c_new = pend.c_new;
+  p.kr_new = pend.kr_new;
+  p.cu_new = pend.cu_new;
+  p.max_new = pend.max_new;
   const cudaError_t e = mlaq::launch_decode(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_QCACHE_OK : MLA_QCACHE_ERR_CUDA;
 }
@@ -333,6 +345,29 @@ int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H, c
                            float* lse, void* workspace, size_t workspace_bytes, int32_t* err_word, void* stream) {
   return decode_impl(cfg, B, H, 1, q_lat, q_rope, page_table, max_pages, seq_lens, pool, n_pages, sink_buf,
                      recent_buf, softmax_scale, out, lse, workspace, workspace_bytes, err_word, stream);
+}
+
+int mla_qcache_decode_attn_pending(const mla_qcache_config* cfg, int32_t B, int32_t H, const uint16_t* q_lat,
+                                   const uint16_t* q_rope, const int32_t* page_table, int32_t max_pages,
+                                   const int32_t* seq_lens, const uint16_t* c_new, const uint16_t* kr_new,
+                                   const int32_t* cu_new, int32_t max_new, const uint8_t* pool, int64_t n_pages,
+                                   const uint16_t* sink_buf, const uint16_t* recent_buf, float softmax_scale,
+                                   float* out, float* lse, void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                   void* stream) {
+  int st = check_config(cfg);
+  if (st != MLA_QCACHE_OK) return st;
+  // the pending rows must lie in the recent window, and every token they push out of it must
+  // already sit in a full page: max_new <= W - P + 1
+  if (max_new < 0 || max_new > cfg->n_recent - cfg->page_size + 1) return MLA_QCACHE_ERR_SHAPE;
+  if (!c_new || !kr_new || !cu_new) return MLA_QCACHE_ERR_NULL;
+  if (!aligned(c_new, 16) || !aligned(kr_new, 16) || !aligned(cu_new, 4)) return MLA_QCACHE_ERR_ALIGN;
+  PendingRows pend;
+  pend.c_new = c_new;
+  pend.kr_new = kr_new;
+  pend.cu_new = cu_new;
+  pend.max_new = max_new;
+  return decode_impl(cfg, B, H, 1, q_lat, q_rope, page_table, max_pages, seq_lens, pool, n_pages, sink_buf,
+                     recent_buf, softmax_scale, out, lse, workspace, workspace_bytes, err_word, stream, pend);
 }
 
 int mla_qcache_decode_attn_multi(const mla_qcache_config* cfg, int32_t B, int32_t H, int32_t q_len,

@@ -243,7 +243,7 @@ __device__ __forceinline__ void load_p(const Shared& sh, int buf, float2 (&pf)[4
 // kPaged: every token of the sequence from a paged BF16 cache (the unquantized comparator);
 // else the sink and recent tokens from the BF16 retention buffers.
 template <bool kPaged>
-__device__ void bf16_split(const DecodeParams& p, const Shared& sh, int b, int T, int part,
+__device__ void bf16_split(const DecodeParams& p, const Shared& sh, int b, int T, int T_old, int part,
                            const uint32_t (&qa)[8][4], const uint32_t (&qra)[4], State& st, int32_t& flags) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Several new tokens per sequence: the CTA's rows belong to position i of the q_len tokens and
@@ -302,7 +302,13 @@ __device__ void bf16_split(const DecodeParams& p, const Shared& sh, int b, int T
     mbar_arrive_expect_tx(bar, kTile * kRow * 2);
     for (int j = 0; j < kTile; ++j) {
       const int t = start + (j < count ? j : 0);  // rows past the count repeat a valid row (masked later)
-      bulk_g2s(dst + j * kBf16RowBytes, row_ptr(t), kRow * 2, bar);
+      if (!kPaged && t >= T_old) {  // a pending row: latent and k_R parts from the write's inputs
+        const size_t r = static_cast<size_t>(__ldg(p.cu_new + b)) + static_cast<size_t>(t - T_old);
+        bulk_g2s(dst + j * kBf16RowBytes, p.c_new + r * kLatent, kLatent * 2, bar);
+        bulk_g2s(dst + j * kBf16RowBytes + kLatent * 2, p.kr_new + r * kRope, kRope * 2, bar);
+      } else {
+        bulk_g2s(dst + j * kBf16RowBytes, row_ptr(t), kRow * 2, bar);
+      }
     }
   };
   if (threadIdx.x == 0) {
@@ -961,7 +967,7 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
 
 // ------------------------------------------------------------------ protected-token CTA
 template <bool kPaged>
-__device__ void protected_split(const DecodeParams& p, const Shared& sh, int b, int T, int part, State& st,
+__device__ void protected_split(const DecodeParams& p, const Shared& sh, int b, int T, int T_old, int part, State& st,
                                 int32_t& flags) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
   const int h0 = blockIdx.y * 16;
@@ -988,7 +994,7 @@ __device__ void protected_split(const DecodeParams& p, const Shared& sh, int b, 
     qra[2] = __ldg(r0 + 4 + q);
     qra[3] = __ldg(r1 + 4 + q);
   }
-  bf16_split<kPaged>(p, sh, b, T, part, qa, qra, st, flags);
+  bf16_split<kPaged>(p, sh, b, T, T_old, part, qa, qra, st, flags);
 
   const int NS = p.n_split + p.n_q, slot = p.n_split + part;
   float* o0 = p.o_part + ((static_cast<size_t>(b) * p.H + h0 + g) * NS + slot) * kLatent + 128 * warp;
@@ -1016,11 +1022,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
   const int h0 = blockIdx.y * 16;
   int32_t flags = 0;
 
-  int T = __ldg(p.seq_lens + b);
-  if (T < 0 || static_cast<long long>(T) > static_cast<long long>(p.max_pages) * p.P) {
-    flags |= kErrSeqOverflow;
-    T = 0;
-  }
+  int T_old;
+  const int T = decode_seq_len(p, b, T_old, flags);
   if (threadIdx.x == 0) {
     if (is_bf16) {  // two row stages, one arrival each
       mbar_init(sh.bars, 1);
@@ -1041,7 +1044,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
   st.m_run = -INFINITY;
   st.l_part = 0.f;
 
-  if (is_bf16) protected_split<kPaged>(p, sh, b, T, split - p.n_split, st, flags);
+  if (is_bf16) protected_split<kPaged>(p, sh, b, T, T_old, split - p.n_split, st, flags);
   else packed_split<BITS, kBalanced>(p, sh, b, T, split, st, flags);
 
   const int NS = p.n_split + p.n_q;

@@ -240,11 +240,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
   const int NS = p.n_split + p.n_q;
   int32_t flags = 0;
 
-  int T = __ldg(p.seq_lens + b);
-  if (T < 0 || static_cast<long long>(T) > static_cast<long long>(p.max_pages) * p.P) {
-    flags |= kErrSeqOverflow;
-    T = 0;
-  }
+  int T_old;
+  const int T = decode_seq_len(p, b, T_old, flags);
   const int lo = p.S, hi = T - p.W;
   int tile_begin = 0, n_my = 0;
   if (hi > lo) {

@@ -91,7 +91,38 @@ struct DecodeParams {
                     // > 0: balanced equal shares (more shares launched than one wave holds)
   int q_len;        // new tokens decoded per sequence (rows [position][head]; 0 or 1: one)
   int h_pos;        // rows per position (H / q_len), a multiple of 16
+  // Rows not yet written to the cache (decode of the cache as the write of these rows will
+  // leave it): sequence b's rows cu_new[b] .. cu_new[b+1]-1 are its tokens seq_lens[b] ..;
+  // cu_new == nullptr: none. They are read from here instead of the sink/recent buffers.
+  const uint16_t* c_new;   // [rows][512] BF16
+  const uint16_t* kr_new;  // [rows][64] BF16
+  const int32_t* cu_new;   // [B+1]
+  int max_new;             // bound on the rows per sequence (larger counts are an error)
 };
+
+#ifdef __CUDACC__
+// Sequence b's length seen by a decode: the cached length plus its pending rows. Out-of-range
+// values set an error bit and count as an empty sequence; `T_old` receives the cached length
+// (the first pending token).
+__device__ __forceinline__ int decode_seq_len(const DecodeParams& p, int b, int& T_old, int32_t& flags) {
+  int T = __ldg(p.seq_lens + b);
+  int n_new = 0;
+  if (p.cu_new != nullptr) {
+    n_new = __ldg(p.cu_new + b + 1) - __ldg(p.cu_new + b);
+    if (n_new < 0 || n_new > p.max_new) {
+      flags |= kErrRows;
+      n_new = 0;
+    }
+  }
+  if (T < 0 || static_cast<long long>(T) + n_new > static_cast<long long>(p.max_pages) * p.P) {
+    flags |= kErrSeqOverflow;
+    T_old = 0;
+    return 0;
+  }
+  T_old = T;
+  return T + n_new;
+}
+#endif
 
 // Number of packed-token shares, and of CTAs for the protected tokens, of each (sequence,
 // 16-head block) for a problem size (depends on the SM count).

@@ -188,6 +188,40 @@ int mla_qcache_write(const mla_qcache_config* cfg, int32_t B, int32_t n_rows,
                      uint16_t* recent_buf, int32_t* err_word, void* stream);
 
 /*
+ * Decode of the cache as a pending write will leave it, without waiting for that write
+ * ([QuantMLA] Figure 8: every token gets a packed copy on arrival and is read from it once it
+ * leaves the recent window). The arguments are those of mla_qcache_decode_attn plus the
+ * write's rows: c_new, kr_new, cu_new and max_new as mla_qcache_write takes them, seq_lens the
+ * lengths BEFORE that write. Sequence b is decoded at length T = seq_lens[b] + (cu_new[b+1] -
+ * cu_new[b]); its pending tokens seq_lens[b] .. T-1 are read from c_new / kr_new (they are the
+ * newest, hence BF16-protected), every other token from the cache.
+ *
+ * Because P <= W, the pending write changes nothing else this decode reads: the packed copies
+ * it adds belong to tokens inside the recent window, a page it fills holds only such tokens,
+ * and the ring slots it overwrites belong to tokens that left the window. So the write
+ * (mla_qcache_write or mla_qcache_write_advance with the same rows and lengths) may run
+ * concurrently on another stream, provided it finishes before the next call that reads this
+ * cache. Only the plain writer qualifies: with a transformed writer the cache holds x A, not
+ * the rows given here.
+ *   max_new    0 <= max_new <= W - P + 1 (1 for a decode step at P = W = 128), so that every
+ *              token the pending rows push out of the window already lies in a full page.
+ *   c_new, kr_new 16-byte aligned; cu_new 4-byte aligned.
+ * Errors: as mla_qcache_decode_attn; bad max_new -> MLA_QCACHE_ERR_SHAPE; a NULL row pointer ->
+ * MLA_QCACHE_ERR_NULL; misaligned rows -> MLA_QCACHE_ERR_ALIGN. On the device, a sequence whose
+ * row count is negative or above max_new sets MLA_QCACHE_DEV_ROWS and is decoded without
+ * pending rows; T beyond max_pages * P sets MLA_QCACHE_DEV_SEQ_OVERFLOW (empty sequence).
+ */
+int mla_qcache_decode_attn_pending(const mla_qcache_config* cfg, int32_t B, int32_t H,
+                                   const uint16_t* q_lat, const uint16_t* q_rope,
+                                   const int32_t* page_table, int32_t max_pages,
+                                   const int32_t* seq_lens, const uint16_t* c_new,
+                                   const uint16_t* kr_new, const int32_t* cu_new, int32_t max_new,
+                                   const uint8_t* pool, int64_t n_pages, const uint16_t* sink_buf,
+                                   const uint16_t* recent_buf, float softmax_scale, float* out,
+                                   float* lse, void* workspace, size_t workspace_bytes,
+                                   int32_t* err_word, void* stream);
+
+/*
  * Decode of several new tokens per sequence in one call (a speculative draft verified in one
  * step, or a short chunk): the q_len tokens are the cache's last ones, written before the
  * call, and position i (0 <= i < q_len) attends to the cache tokens t < T - (q_len - 1 - i),

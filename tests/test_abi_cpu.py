@@ -254,3 +254,21 @@ def test_binding_rejects_bad_shapes_before_any_call(L):
         with pytest.raises(ValueError):
             binding.mla_qcache_decode_attn_noalloc(cfg, a["q_lat"], a["q_rope"], a["page_table"], a["seq_lens"], None, None,
                                              None, 0.1, a["out"], a["lse"], None)
+
+
+def test_pending_decode_validates_on_the_host(L):
+    """mla_qcache_decode_attn_pending: max_new beyond W - P + 1, missing or misaligned row
+    pointers are rejected before any launch; the decode's own checks still apply."""
+    lib = L.lib()
+    p, odd = ctypes.c_void_p(16 * 1024), ctypes.c_void_p(16 * 1024 + 8)
+    f = ctypes.c_float(0.1)
+    call = lambda cfg, H, c, k, cu, mx: lib.mla_qcache_decode_attn_pending(
+        ctypes.byref(cfg), 1, H, p, p, p, 1, p, c, k, cu, mx, p, 1, p, p, f, p, p, p, 1 << 20, p, None)
+    c4 = L.make_config(4, 128)                 # W - P + 1 = 1
+    c32 = L.make_config(4, 32, n_recent=128)   # W - P + 1 = 97
+    assert call(c4, 16, p, p, p, 2) == -3 and call(c4, 16, p, p, p, -1) == -3
+    assert call(c32, 16, p, p, p, 98) == -3
+    assert call(c4, 16, None, p, p, 1) == -1 and call(c4, 16, p, None, p, 1) == -1 and call(c4, 16, p, p, None, 1) == -1
+    assert call(c4, 16, odd, p, p, 1) == -4 and call(c4, 16, p, odd, p, 1) == -4
+    assert call(c4, 24, p, p, p, 1) == -3  # H not a multiple of 16
+    assert call(L.make_config(4, 128, n_recent=64), 16, p, p, p, 1) == -2
