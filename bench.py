@@ -479,10 +479,14 @@ def measure_workload(args, w, q, dev, steps, warmup, layers, with_e2e):
             for lens_in, lens_out in ((cache.seq_lens, alt), (alt, cache.seq_lens)):
                 gs = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(gs, stream=stream):
-                    write_stream.wait_stream(stream)
+                    # the writer forks from the step's start; the decode's node is created first
+                    # (measured: the writer then delays the decode's one wave of CTAs less)
+                    ev_fork = torch.cuda.Event()
+                    ev_fork.record(stream)
+                    pending_step(cache, lens_in)
+                    write_stream.wait_event(ev_fork)
                     with torch.cuda.stream(write_stream):
                         write_step(cache, lens_in, lens_out)
-                    pending_step(cache, lens_in)
                     stream.wait_stream(write_stream)
                 pair.append(gs)
             gd = torch.cuda.CUDAGraph()
@@ -632,12 +636,14 @@ def e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream):
             stream.wait_event(ev_h2d[k])
             if k >= 2:
                 stream.wait_event(ev_d2h[k - 2])  # step k-2's results have left this output slot
-            s_wr.wait_stream(stream)  # the write forks off after the step's inputs arrived
-            q.mla_qcache_write_advance(cfg, d_c, d_k, cu1, lens_in, lens_out, 1, cache.page_table, cache.pool,
-                                       cache.sink, cache.ring, cache.err, s_wr)
+            ev_fork = torch.cuda.Event()
+            ev_fork.record(stream)  # the write forks off once the step's inputs arrived
             q.mla_qcache_decode_attn_pending(cfg, d_ql, d_qr, cache.page_table, lens_in, d_c, d_k, cu1, 1, cache.pool,
                                              cache.sink, cache.ring, w.softmax_scale, out, lse, ws_buf, cache.err,
                                              stream)
+            s_wr.wait_event(ev_fork)
+            q.mla_qcache_write_advance(cfg, d_c, d_k, cu1, lens_in, lens_out, 1, cache.page_table, cache.pool,
+                                       cache.sink, cache.ring, cache.err, s_wr)
             stream.wait_stream(s_wr)  # joined: the next step reads what this write stored
             ev_comp[k].record(stream)
             with torch.cuda.stream(s_out):

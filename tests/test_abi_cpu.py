@@ -192,9 +192,16 @@ def test_decode_plan_shapes(L):
     for mp in (514, 2050, 8194):
         p = L.decode_plan(c4, 1, 16, mp, sms)
         assert p["n_split"] == wave - 1 and p["share_slots"] == 0
-    # a short table: at least four 32-token tiles per share
-    p = L.decode_plan(c4, 1, 16, 10, sms)
+    # the minimum share: four 32-token tiles, except for one or two sequence-head groups: one
+    # tile for short tables (up to 96 tiles), two up to 384, four beyond
+    p = L.decode_plan(c4, 8, 16, 10, sms)
     assert p["n_split"] == 10 * 128 // 32 // 4
+    p = L.decode_plan(c4, 1, 16, 10, sms)
+    assert p["n_split"] == 10 * 128 // 32
+    p = L.decode_plan(c4, 1, 16, 66, sms)
+    assert p["n_split"] == 66 * 128 // 32 // 2
+    p = L.decode_plan(c4, 1, 16, 130, sms)
+    assert p["n_split"] == 130 * 128 // 32 // 4
     # eight long sequences: more shares than a wave, in the balanced instance
     p = L.decode_plan(c4, 8, 16, 8194, sms)
     assert p["n_split"] == 64 and p["share_slots"] == wave - 8 * p["n_protected"]
