@@ -294,24 +294,29 @@ __device__ void bf16_split(const DecodeParams& p, const Shared& sh, int b, int T
                      : p.ring + (static_cast<size_t>(b) * p.W + (t % p.W)) * kRow;
     }
   };
+  // Warp 0 stages tile i: lane 0 announces the stage's bytes, then lanes 0-15 each copy one row
+  // (its address lookup and copy run in parallel rather than one after another).
   auto issue = [&](int i) {
     int start, count;
     tile_range(i, start, count);
     uint8_t* dst = sh.stages + (i & 1) * kStageBytes;
     uint64_t* bar = sh.bars + (i & 1);
-    mbar_arrive_expect_tx(bar, kTile * kRow * 2);
-    for (int j = 0; j < kTile; ++j) {
-      const int t = start + (j < count ? j : 0);  // rows past the count repeat a valid row (masked later)
-      if (!kPaged && t >= T_old) {  // a pending row: latent and k_R parts from the write's inputs
-        const size_t r = static_cast<size_t>(__ldg(p.cu_new + b)) + static_cast<size_t>(t - T_old);
-        bulk_g2s(dst + j * kBf16RowBytes, p.c_new + r * kLatent, kLatent * 2, bar);
-        bulk_g2s(dst + j * kBf16RowBytes + kLatent * 2, p.kr_new + r * kRope, kRope * 2, bar);
-      } else {
-        bulk_g2s(dst + j * kBf16RowBytes, row_ptr(t), kRow * 2, bar);
-      }
+    if (lane == 0) mbar_arrive_expect_tx(bar, kTile * kRow * 2);
+    __syncwarp();
+    // lanes 0-15: row `lane` from the cache; lanes 16-31: row `lane - 16` when it is pending (its
+    // latent and k_R parts from the write's inputs)
+    const int j = lane & (kTile - 1);
+    const int t = start + (j < count ? j : 0);  // rows past the count repeat a valid row (masked later)
+    const bool pend = !kPaged && t >= T_old;
+    if (lane < kTile) {
+      if (!pend) bulk_g2s(dst + j * kBf16RowBytes, row_ptr(t), kRow * 2, bar);
+    } else if (pend) {
+      const size_t r = static_cast<size_t>(__ldg(p.cu_new + b)) + static_cast<size_t>(t - T_old);
+      bulk_g2s(dst + j * kBf16RowBytes, p.c_new + r * kLatent, kLatent * 2, bar);
+      bulk_g2s(dst + j * kBf16RowBytes + kLatent * 2, p.kr_new + r * kRope, kRope * 2, bar);
     }
   };
-  if (threadIdx.x == 0) {
+  if (warp == 0) {
     issue(0);
     if (n_tiles > 1) issue(1);
   }
@@ -379,7 +384,7 @@ __device__ void bf16_split(const DecodeParams& p, const Shared& sh, int b, int T
       mma_bf16_16816(st.o[2 * kc + 1], A_lo, r[2], r[3]);
     }
     __syncthreads();  // every warp is done with this stage before it is refilled
-    if (threadIdx.x == 0 && i + 2 < n_tiles) {
+    if (warp == 0 && i + 2 < n_tiles) {
       fence_proxy_async_smem();
       issue(i + 2);
     }
