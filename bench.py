@@ -368,7 +368,7 @@ def config_dict(w, layers):
 # ------------------------------------------------------------------ GPU arm
 
 EXTRA_WORKLOADS = ("v2lite_c4r4_b32_h16_t32k", "ragged_c2r4_b64_h16_serve", "wide_c2r4_b8_h128_t32k",
-                   "long_c4r4_b1_h128_t128k")
+                   "long_c4r4_b1_h128_t128k", "tiny_c4r4_b1_h16_t1k")
 
 
 def run_native(args, w):
