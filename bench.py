@@ -543,6 +543,7 @@ def measure_workload(args, w, q, dev, steps, warmup, layers, with_e2e):
     achieved = bytes_dec / (dec_us * 1e-6) / 1e9
     tflops = flops_dec / (dec_us * 1e-6) / 1e12
     traffic = profiled_traffic(w.name)
+    dec_launches = q.decode_launches(cfg, B, H, max_pages)
     if H % 64 == 0:
         # 64-head blocks run the packed tokens on tcgen05 tensor cores; at ~1000 flops per packed
         # byte the decode is bound by the tensor pipe, not by HBM
@@ -551,13 +552,15 @@ def measure_workload(args, w, q, dev, steps, warmup, layers, with_e2e):
                     "kernel": "mla_qcache_decode_attn (decode_tc_kernel + protected decode_kernel + combine_kernel)",
                     "algorithmic_flops_per_call": flops_dec, "algorithmic_bytes_per_call": bytes_dec,
                     "hbm_frac": achieved / hbm_peak, "peak_kind": peak_kind}
-        launches_per_step = 4  # fused write + length update, protected decode, tensor-core decode, merge
     else:
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                     "frac": achieved / hbm_peak, "traffic": traffic,
-                    "kernel": "mla_qcache_decode_attn (decode_kernel + combine_kernel)",
+                    "kernel": "mla_qcache_decode_attn (decode_kernel" +
+                              (" with the partials merged in place)" if dec_launches == 1 else " + combine_kernel)"),
                     "algorithmic_bytes_per_call": bytes_dec, "peak_kind": peak_kind}
-        launches_per_step = 3  # fused write + length update, decode, merge
+    # the fused write + length update, then the decode's own launches (decode with the merge in
+    # place; decode + merge; or protected decode + tensor-core decode + merge)
+    launches_per_step = 1 + dec_launches
 
     result = {
         "metric": METRIC, "value": us_step * 1.0, "unit": "us/layer", "n_gpus": ws, "steps": steps,
@@ -781,7 +784,7 @@ def run_sweep(args):
                 del rows, tok
                 err = torch.zeros(1, dtype=torch.int32, device=dev)
                 ws_q = cache.workspace(H)
-                ws_b = torch.empty(q.bf16_workspace_bytes(B, H, mp_b, P_b), dtype=torch.uint8, device=dev)
+                ws_b = torch.zeros(q.bf16_workspace_bytes(B, H, mp_b, P_b), dtype=torch.uint8, device=dev)
                 torch.cuda.synchronize()
                 if cache.error_bits():
                     raise RuntimeError("writer reported device errors while building the sweep cache")
@@ -943,7 +946,7 @@ def run_multi(args):
                 d_ql, d_qr = to_dev(ql), to_dev(qr)
                 out = torch.empty((B, R, 512), dtype=torch.float32, device=dev)
                 lse = torch.empty((B, R), dtype=torch.float32, device=dev)
-                ws = torch.empty(q.workspace_bytes(cfg, B, R, inp.page_table.shape[1]), dtype=torch.uint8, device=dev)
+                ws = torch.zeros(q.workspace_bytes(cfg, B, R, inp.page_table.shape[1]), dtype=torch.uint8, device=dev)
                 fn = lambda: q.mla_qcache_decode_attn_multi(cfg, q_len, d_ql, d_qr, cache.page_table, cache.seq_lens,
                                                             cache.pool, cache.sink, cache.ring, w.softmax_scale, out,
                                                             lse, ws, cache.err)

@@ -24,7 +24,7 @@ EXPORTS = ("mla_qcache_page_bytes", "mla_qcache_config_check", "mla_qcache_works
            "mla_qcache_write_advance", "mla_qcache_decode_attn_bf16", "mla_qcache_bf16_workspace_bytes",
            "mla_qcache_write_transformed", "mla_qcache_row_transform", "mla_qcache_absorb_query",
            "mla_qcache_up_project", "mla_qcache_decode_attn_multi", "mla_qcache_decode_plan",
-           "mla_qcache_selftest_wait_timeout", "mla_qcache_decode_attn_pending")
+           "mla_qcache_selftest_wait_timeout", "mla_qcache_decode_attn_pending", "mla_qcache_decode_launches")
 
 
 class Config(ctypes.Structure):
@@ -87,6 +87,8 @@ def lib() -> ctypes.CDLL:
         L.mla_qcache_selftest_wait_timeout.argtypes = [vp, vp]
         L.mla_qcache_decode_plan.restype = ctypes.c_int
         L.mla_qcache_decode_plan.argtypes = [P(Config), i32, i32, i32, i32, P(i32)]
+        L.mla_qcache_decode_launches.restype = ctypes.c_int
+        L.mla_qcache_decode_launches.argtypes = [P(Config), i32, i32, i32]
         L.mla_qcache_decode_attn_pending.restype = ctypes.c_int
         L.mla_qcache_decode_attn_pending.argtypes = [P(Config), i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, i32, vp, i64,
                                                      vp, vp, ctypes.c_float, vp, vp, vp, sz, vp, vp]
@@ -244,6 +246,14 @@ def decode_plan(cfg: Config, B: int, H: int, max_pages: int, num_sms: int) -> di
     _raise(lib().mla_qcache_decode_plan(ctypes.byref(cfg), B, H, max_pages, num_sms, out), "mla_qcache_decode_plan")
     return {"n_split": out[0], "n_protected": out[1], "share_slots": out[2], "tensor_memory": bool(out[3]),
             "bf16_parts": out[4]}
+
+
+def decode_launches(cfg: Config, B: int, H: int, max_pages: int) -> int:
+    """Kernel launches of one decode call of this shape on the current device (see
+    include/mla_qcache.h): 1 (merged in place), 2 (with a merge launch) or 3 (64-head blocks)."""
+    n = lib().mla_qcache_decode_launches(ctypes.byref(cfg), B, H, max_pages)
+    _raise(min(n, 0), "mla_qcache_decode_launches")
+    return n
 
 
 def mla_qcache_decode_attn_multi(cfg: Config, q_len: int, q_lat, q_rope, page_table, seq_lens, pool, sink_buf,

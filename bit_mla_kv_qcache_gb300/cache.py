@@ -62,7 +62,8 @@ class QuantizedMLACache:
         if need is None:
             need = self._ws_need[heads] = binding.workspace_bytes(self.cfg, self.B, heads, self.max_pages)
         if self._ws is None or self._ws.numel() < need:
-            self._ws = torch.empty(max(need, 16), dtype=torch.uint8, device=self.pool.device)
+            # zeroed once: the decode keeps the merge counters at its start zero between calls
+            self._ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=self.pool.device)
         return self._ws
 
     def decode(self, q_lat: torch.Tensor, q_rope: torch.Tensor, softmax_scale: float, out=None, lse=None,

@@ -218,6 +218,20 @@ int mla_qcache_decode_plan(const mla_qcache_config* cfg, int32_t B, int32_t H, i
   return MLA_QCACHE_OK;
 }
 
+int mla_qcache_decode_launches(const mla_qcache_config* cfg, int32_t B, int32_t H, int32_t max_pages) {
+  const int st = check_config(cfg);
+  if (st != MLA_QCACHE_OK) return st;
+  if (B < 1 || B > 65535 || H < 16 || H > 256 || H % 16 || max_pages < 1) return MLA_QCACHE_ERR_SHAPE;
+  int sms = 0;
+  const int st2 = current_sm_count(&sms);
+  if (st2 != MLA_QCACHE_OK) return st2;
+  const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, sms);
+  const int nq = mlaq::decode_num_protected(B, H, max_pages, cfg->page_size, cfg->n_sink, cfg->n_recent, sms);
+  const int slots = mlaq::decode_share_slots(B, H, max_pages, cfg->page_size, ns, nq, sms);
+  const int n = mlaq::decode_launch_count(cfg->bits_c, B, H, ns, nq, slots);
+  return n > 0 ? n : MLA_QCACHE_ERR_CUDA;
+}
+
 int mla_qcache_absorb_query(int32_t B, int32_t H, int32_t d_nope, const uint16_t* q_nope, const uint16_t* w_uk,
                             const uint16_t* q_rope, const uint16_t* r_comp, uint16_t* q_lat, uint16_t* q_rope_out,
                             void* stream) {
@@ -306,8 +320,9 @@ static int decode_impl(const mla_qcache_config* cfg, int32_t B, int32_t H, int32
   p.pool = pool;
   p.sink = sink_buf;
   p.ring = recent_buf;
-  p.o_part = static_cast<float*>(workspace);
-  p.ml_part = static_cast<float*>(workspace) + static_cast<size_t>(B) * H * (ns + nq) * mlaq::kLatent;
+  p.arrive = static_cast<unsigned long long*>(workspace);
+  p.o_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + mlaq::kArriveBytes);
+  p.ml_part = p.o_part + static_cast<size_t>(B) * H * (ns + nq) * mlaq::kLatent;
   p.out = out;
   p.lse = lse;
   p.err = err_word;
@@ -414,8 +429,9 @@ int mla_qcache_decode_attn_bf16(int32_t B, int32_t H, const uint16_t* q_lat, con
   p.page_table = page_table;
   p.seq_lens = seq_lens;
   p.kv_bf16 = kv_pool;
-  p.o_part = static_cast<float*>(workspace);
-  p.ml_part = static_cast<float*>(workspace) + static_cast<size_t>(B) * H * parts * mlaq::kLatent;
+  p.arrive = static_cast<unsigned long long*>(workspace);
+  p.o_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + mlaq::kArriveBytes);
+  p.ml_part = p.o_part + static_cast<size_t>(B) * H * parts * mlaq::kLatent;
   p.out = out;
   p.lse = lse;
   p.err = err_word;

@@ -1011,6 +1011,142 @@ __device__ void protected_split(const DecodeParams& p, const Shared& sh, int b, 
   }
 }
 
+// ------------------------------------------------------------------ in-kernel merge
+// When the whole grid is one resident wave, the NS CTAs of a (sequence, 16-head block) may merge
+// their own partials (when the partials are many: see in_place_merge). The block's counter is one 64-bit word: arrivals in the low half (zero
+// between calls), a generation in the high half. Each CTA, once its partial is stored (CTA
+// barrier first), adds one arrival (release of the CTA's stores, acquire of the earlier
+// arrivals'); the last arrival adds 2^32 - NS, which clears the count and advances the
+// generation in one step; the others wait (bounded) until they see the count complete or the
+// generation moved. No CTA can keep a waiting one's group from running: every CTA is
+// resident. Returns false if the wait gave up or the count was not a valid arrival count (a
+// workspace whose counters were not zero): the partials may then be incomplete.
+__device__ __forceinline__ bool group_arrive(unsigned long long* ctr, int NS) {
+  const unsigned long long old = atom_add_acq_rel_gpu(ctr, 1ull);
+  const uint32_t t = static_cast<uint32_t>(old), g0 = static_cast<uint32_t>(old >> 32);
+  if (t >= static_cast<uint32_t>(NS)) return false;
+  if (t == static_cast<uint32_t>(NS - 1)) {
+    red_add_release_gpu(ctr, (1ull << 32) - static_cast<unsigned long long>(NS));
+    return true;
+  }
+  // released by the last arrival itself (count NS, reached before the reset is seen) or by the
+  // reset (generation moved); the acquire of either orders every arrival's stores before ours
+  const long long t0 = clock64();
+  for (;;) {
+    const unsigned long long v = ld_acquire_gpu(ctr);
+    if (static_cast<uint32_t>(v >> 32) != g0 || static_cast<uint32_t>(v) == static_cast<uint32_t>(NS)) return true;
+    if (clock64() - t0 > kWaitBudget) return false;
+    __nanosleep(32);
+  }
+}
+
+// The merge of one (sequence, 16-head block)'s NS partials by CTA z of its n_ctas: float4
+// columns [z*2048/n_ctas, (z+1)*2048/n_ctas) of the block's output (16 heads x 128 columns). The slice of every
+// partial and the partial maxima and sums of the slice's heads are first copied into shared
+// memory, all requests in flight at once (16-byte asynchronous copies through L2: the partials
+// were stored by other SMs during this launch). One warp per head then forms the head's
+// maximum M and sum L = sum_s 2^(m_s - M) l_s and turns each partial's (m_s, l_s) into its weight
+// 2^(m_s - M) / L (and writes the head's log-sum-exp if the slice holds its first column); R
+// lanes take one column (R a power of two, as many as fill the CTA), each summing every R-th
+// weighted partial, and shuffles add the R sums. Partials of empty shares (maximum -inf) have
+// weight 0 and are selected out, never multiplied: their rows hold whatever the buffer held.
+// `buf` holds merge_buf_need(NS, n_ctas) bytes (checked on the host): NS partial slots merged by
+// the group's n_ctas CTAs.
+__host__ __device__ constexpr int merge_buf_need(int NS, int n_ctas) {
+  return NS * (2048 / n_ctas + 1) * 16 + ((2048 / n_ctas) / 128 + 2) * NS * 8 + 32 + 256;
+}
+
+__device__ __forceinline__ void group_merge(const DecodeParams& p, uint8_t* buf, int b, int h0, int z, int n_ctas,
+                                            int NS) {
+  constexpr int kCols = 16 * (kLatent / 4);
+  const int c0 = static_cast<int>(static_cast<long long>(z) * kCols / n_ctas);
+  const int c1 = static_cast<int>(static_cast<long long>(z + 1) * kCols / n_ctas);
+  const int n_cols = c1 - c0;
+  if (n_cols <= 0) return;  // (uniform in the CTA)
+  const int hA = c0 >> 7, n_h = ((c1 - 1) >> 7) - hA + 1;
+  const size_t bh0 = static_cast<size_t>(b) * p.H + h0;
+  // (m_s, l_s) of the slice's heads: [n_h][NS] pairs, contiguous in the partial maxima and sums;
+  // copied as the enclosing 16-byte blocks (the array starts 16-byte aligned and the workspace
+  // holds 16 bytes beyond it), so the rows start 0 or 8 bytes into the copy
+  const size_t ml0 = (bh0 + hA) * NS * 2;  // float index of the first pair
+  const float* mlg = p.ml_part + (ml0 & ~static_cast<size_t>(3));
+  const int n_ml16 = static_cast<int>(((ml0 & 3) * 4 + static_cast<size_t>(n_h) * NS * 8 + 15) / 16);
+  float2* mls = reinterpret_cast<float2*>(buf + (ml0 & 3) * 4);  // [n_h][NS]: (m_s, l_s), then (weight, -)
+  float4* os = reinterpret_cast<float4*>(buf + n_ml16 * 16);      // [NS][n_cols]
+  for (int j = threadIdx.x; j < n_ml16; j += kThreads) cp_async_cg16(buf + j * 16, mlg + 4 * j);
+  // thread -> (column, every k-th partial): k = 1 when the columns alone fill the CTA
+  const int k = n_cols >= kThreads ? 1 : kThreads / n_cols;
+  const int s_first = n_cols >= kThreads ? 0 : static_cast<int>(threadIdx.x) / n_cols;
+  if (s_first < k)
+    for (int ci = static_cast<int>(threadIdx.x) - s_first * n_cols; ci < n_cols; ci += kThreads) {
+      const int c = c0 + ci;
+      const float* src = p.o_part + (bh0 + (c >> 7)) * NS * kLatent + 4 * (c & 127);
+      for (int s = s_first; s < NS; s += k) cp_async_cg16(os + s * n_cols + ci, src + static_cast<size_t>(s) * kLatent);
+    }
+  cp_async_wait_all();
+  __syncthreads();
+  // per-head weights (warp w: heads w, w+4, ...)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int hh = warp; hh < n_h; hh += kThreads / 32) {
+    float2* row = mls + hh * NS;
+    float m = -INFINITY;
+    for (int s = lane; s < NS; s += 32) m = fmaxf(m, row[s].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float l = 0.f;
+    if (m != -INFINITY)
+      for (int s = lane; s < NS; s += 32) l += exp2f(row[s].x - m) * row[s].y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    const bool any = m != -INFINITY && l > 0.f;
+    const float inv = any ? 1.f / l : 0.f;
+    __syncwarp();
+    for (int s = lane; s < NS; s += 32) row[s].x = any ? exp2f(row[s].x - m) * inv : 0.f;
+    if (lane == 0 && ((hA + hh) << 7) >= c0)  // the slice holds the head's first column
+      p.lse[bh0 + hA + hh] = any ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+  }
+  __syncthreads();
+
+  int lg = 0;  // R = 2^lg lanes per column
+  while (lg < 5 && (n_cols << (lg + 1)) <= kThreads) ++lg;
+  const int R = 1 << lg, per_pass = kThreads >> lg;
+  const int slot = static_cast<int>(threadIdx.x) >> lg, r = static_cast<int>(threadIdx.x) & (R - 1);
+  const int n_pass = (n_cols + per_pass - 1) / per_pass;
+  for (int pass = 0; pass < n_pass; ++pass) {
+    const int ci = pass * per_pass + slot;  // column within the slice
+    const bool active = ci < n_cols;
+    const int c = c0 + ci;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (active) {
+      const float2* wrow = mls + ((c >> 7) - hA) * NS;
+#pragma unroll 4
+      for (int s = r; s < NS; s += R) {
+        const float w = wrow[s].x;
+        if (w == 0.f) continue;
+        const float4 v = os[s * n_cols + ci];
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+      }
+    }
+    for (int o = 1; o < R; o <<= 1) {
+      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
+      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, o);
+      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
+      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
+    }
+    if (active && r == 0) *reinterpret_cast<float4*>(p.out + (bh0 + (c >> 7)) * kLatent + 4 * (c & 127)) = acc;
+  }
+}
+
+// Bytes of a 16-head CTA's shared memory free for the merge once its shares are done: the stage
+// region and the two exchange buffers that follow it (the barriers lie beyond).
+template <int BITS>
+__host__ __device__ constexpr int merge_buf_bytes() {
+  return Geom<BITS>::kRegion + (kXsFloats + kXpFloats) * 4;
+}
+
 // kBalanced: equal shares sized from the whole batch (launched when more shares than one wave
 // are needed); a separate instance, so the one-wave kernel carries none of its code.
 template <int BITS, bool kBalanced, bool kPaged = false>
@@ -1061,6 +1197,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
     float* ml = p.ml_part + ((static_cast<size_t>(b) * p.H + hh) * NS + split) * 2;
     ml[0] = st.m_run;
     ml[1] = l_run;
+  }
+  if (!kBalanced && p.arrive != nullptr) {  // the grid is one resident wave: merge in place
+    __syncthreads();  // the CTA's partial stores precede its arrival
+    // (indices re-read from the launch: nothing stays live across the main loop for this)
+    int ok = 0;
+    if (threadIdx.x == 0) ok = group_arrive(p.arrive + (blockIdx.x * gridDim.y + blockIdx.y), gridDim.z);
+    if (__syncthreads_or(ok))
+      group_merge(p, sh.stages, blockIdx.x, blockIdx.y * 16, blockIdx.z, gridDim.z, p.n_split + p.n_q);
+    else flags |= kErrTimeout;
   }
   flags = __reduce_or_sync(0xffffffffu, flags);
   if (lane == 0 && flags) atomicOr(p.err, flags);
@@ -1254,54 +1399,131 @@ int decode_share_slots(int B, int H, int max_pages, int P, int n_split, int n_q,
 
 size_t decode_workspace_bytes(int B, int H, int n_slots) {
   const size_t NS = static_cast<size_t>(n_slots);
-  return static_cast<size_t>(B) * H * NS * (kLatent + 2) * sizeof(float);
+  // (+16: the merge copies the partial maxima and sums in whole 16-byte blocks)
+  return kArriveBytes + static_cast<size_t>(B) * H * NS * (kLatent + 2) * sizeof(float) + 16;
 }
 
-// The dynamic shared-memory opt-in is a per-device function attribute: set it once per device
-// (never inside a stream capture after the first call).
-template <int BITS, bool kBalanced>
-cudaError_t ensure_smem_attr() {
-  static bool done[64] = {};
+namespace {
+
+// Per-device launch facts of one decode kernel instance, looked up once (never inside a stream
+// capture after the first call): the dynamic shared-memory opt-in is a function attribute, and
+// the in-kernel merge needs the resident CTAs per SM and the SM count.
+struct Residency {
+  int per_sm;
+  int sms;
+};
+template <int BITS, bool kBalanced, bool kPaged>
+cudaError_t ensure_decode_setup(Residency* out) {
+  static std::atomic<int> per_sm[64], sms[64];  // 0: not yet set up
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!done[dev]) {
-    e = cudaFuncSetAttribute(decode_kernel<BITS, kBalanced>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (per_sm[dev].load(std::memory_order_acquire) == 0) {
+    e = cudaFuncSetAttribute(decode_kernel<BITS, kBalanced, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes<BITS>());
     if (e != cudaSuccess) return e;
-    done[dev] = true;
+    int n = 0, m = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<BITS, kBalanced, kPaged>, kThreads,
+                                                      smem_bytes<BITS>());
+    if (e != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&m, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    sms[dev].store(m, std::memory_order_relaxed);
+    per_sm[dev].store(n > 0 ? n : -1, std::memory_order_release);
   }
+  const int n = per_sm[dev].load(std::memory_order_acquire);
+  out->per_sm = n > 0 ? n : 0;
+  out->sms = sms[dev].load(std::memory_order_relaxed);
   return cudaSuccess;
 }
 
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
-  // 64-head blocks: the packed shares run on the tensor-memory kernel, the protected shares here
-  const bool tc = decode_uses_tc(p.H);
-  const dim3 grid(p.B, p.H / 16, tc ? p.n_q : p.n_q + p.n_split);
-  cudaError_t e;
-  const bool bal = !tc && p.share_slots > 0;
-  if (p.bits_c == 4) {
-    if (bal) {
-      if ((e = ensure_smem_attr<4, true>()) != cudaSuccess) return e;
-      decode_kernel<4, true><<<grid, kThreads, smem_bytes<4>(), stream>>>(p);
-    } else {
-      if ((e = ensure_smem_attr<4, false>()) != cudaSuccess) return e;
-      decode_kernel<4, false><<<grid, kThreads, smem_bytes<4>(), stream>>>(p);
-    }
-  } else {
-    if (bal) {
-      if ((e = ensure_smem_attr<2, true>()) != cudaSuccess) return e;
-      decode_kernel<2, true><<<grid, kThreads, smem_bytes<2>(), stream>>>(p);
-    } else {
-      if ((e = ensure_smem_attr<2, false>()) != cudaSuccess) return e;
-      decode_kernel<2, false><<<grid, kThreads, smem_bytes<2>(), stream>>>(p);
-    }
-  }
-  e = cudaGetLastError();
+// Whether a 16-head launch of `grid` (n_slots partials per sequence-head group) merges its
+// partials in place: the grid must be one resident wave (so that a CTA waiting for its group
+// cannot keep the others from running), the workspace must have a counter per group and the
+// free shared memory must hold a CTA's slice of the partials; and the partials must be many
+// (at least kMinInPlaceSlots per group). With few partials per group the merge launch is as
+// fast: the in-place merge's chain of device-wide round trips (arrival, release, copies) costs
+// about what the separate launch does (measured on GB300: in place wins from ~24 partials per
+// group, loses ~1 us at 14).
+constexpr int kMinInPlaceSlots = 24;
+template <int BITS, bool kPaged>
+cudaError_t in_place_merge(dim3 grid, int n_slots, bool* yes) {
+  Residency res{};
+  const cudaError_t e = ensure_decode_setup<BITS, false, kPaged>(&res);
   if (e != cudaSuccess) return e;
-  if (tc && (e = launch_decode_tc(p, stream)) != cudaSuccess) return e;
+  const long long groups = static_cast<long long>(grid.x) * grid.y;
+  const long long ctas = groups * grid.z;
+  *yes = groups <= kMaxArriveGroups && ctas <= static_cast<long long>(res.per_sm) * res.sms &&
+         n_slots >= kMinInPlaceSlots && merge_buf_need(n_slots, static_cast<int>(grid.z)) <= merge_buf_bytes<BITS>();
+  return cudaSuccess;
+}
+
+// Launch of the 16-head kernel, merging the partials in place (a cooperative launch, which
+// guarantees that every CTA is resident at once) or by a merge launch after it.
+template <int BITS, bool kBalanced, bool kPaged>
+cudaError_t launch_decode_kernel(DecodeParams p, dim3 grid, cudaStream_t stream) {
+  Residency res{};
+  cudaError_t e = ensure_decode_setup<BITS, kBalanced, kPaged>(&res);
+  if (e != cudaSuccess) return e;
+  bool fused = false;
+  if (!kBalanced && p.arrive != nullptr &&
+      (e = in_place_merge<BITS, kPaged>(grid, p.n_split + p.n_q, &fused)) != cudaSuccess)
+    return e;
+  if (!fused) p.arrive = nullptr;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes<BITS>();
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = fused ? 1 : 0;
+  if ((e = cudaLaunchKernelEx(&cfg, decode_kernel<BITS, kBalanced, kPaged>, p)) != cudaSuccess) return e;
+  if (fused) return cudaSuccess;
   return launch_combine(p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
+  // 64-head blocks: the packed shares run on the tensor-memory kernel, the protected shares here,
+  // and a merge launch follows both
+  const bool tc = decode_uses_tc(p.H);
+  if (tc) {
+    DecodeParams q = p;
+    q.arrive = nullptr;
+    const dim3 grid(p.B, p.H / 16, p.n_q);
+    cudaError_t e;
+    Residency res{};
+    if (p.bits_c == 4) {
+      if ((e = ensure_decode_setup<4, false, false>(&res)) != cudaSuccess) return e;
+      decode_kernel<4, false><<<grid, kThreads, smem_bytes<4>(), stream>>>(q);
+    } else {
+      if ((e = ensure_decode_setup<2, false, false>(&res)) != cudaSuccess) return e;
+      decode_kernel<2, false><<<grid, kThreads, smem_bytes<2>(), stream>>>(q);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_decode_tc(q, stream)) != cudaSuccess) return e;
+    return launch_combine(q, stream);
+  }
+  const dim3 grid(p.B, p.H / 16, p.n_q + p.n_split);
+  const bool bal = p.share_slots > 0;  // balanced shares: more than one wave, never merged in place
+  if (p.bits_c == 4)
+    return bal ? launch_decode_kernel<4, true, false>(p, grid, stream) : launch_decode_kernel<4, false, false>(p, grid, stream);
+  return bal ? launch_decode_kernel<2, true, false>(p, grid, stream) : launch_decode_kernel<2, false, false>(p, grid, stream);
+}
+
+int decode_launch_count(int bits_c, int B, int H, int n_split, int n_q, int share_slots) {
+  if (decode_uses_tc(H)) return 3;
+  if (share_slots > 0) return 2;
+  const dim3 grid(B, H / 16, n_q + n_split);
+  bool fused = false;
+  const cudaError_t e = bits_c == 4 ? in_place_merge<4, false>(grid, n_split + n_q, &fused)
+                                    : in_place_merge<2, false>(grid, n_split + n_q, &fused);
+  if (e != cudaSuccess) return -1;
+  return fused ? 1 : 2;
 }
 
 // The unquantized comparator: every share a BF16 share over the paged BF16 cache.
@@ -1324,21 +1546,7 @@ int decode_bf16_num_parts(int B, int H, int max_pages, int P, int num_sms) {
 }
 
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t stream) {
-  static bool done[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!done[dev]) {
-    e = cudaFuncSetAttribute(decode_kernel<4, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_bytes<4>());
-    if (e != cudaSuccess) return e;
-    done[dev] = true;
-  }
-  const dim3 grid(p.B, p.H / 16, p.n_q);
-  decode_kernel<4, false, true><<<grid, kThreads, smem_bytes<4>(), stream>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  return launch_combine(p, stream);
+  return launch_decode_kernel<4, false, true>(p, dim3(p.B, p.H / 16, p.n_q), stream);
 }
 
 // ------------------------------------------------------------------ built-in scratch

@@ -75,6 +75,10 @@ struct DecodeParams {
   const uint16_t* sink;
   const uint16_t* ring;
   const uint16_t* kv_bf16;  // paged BF16 cache of the unquantized comparator (else nullptr)
+  // Arrival counters of the in-kernel merge, one 64-bit word per (sequence, 16-head block):
+  // count (low half, zero between calls) and generation (high half), in the workspace's first
+  // kArriveBytes. nullptr: the partials are merged by a separate launch.
+  unsigned long long* arrive;
   float* o_part;  // [B][H][NS][512] partial (unnormalized) outputs
   float* ml_part; // [B][H][NS][2] partial (max in log2 units, sum)
   float* out;     // [B][H][512]
@@ -128,6 +132,10 @@ __device__ __forceinline__ int decode_seq_len(const DecodeParams& p, int b, int&
 // 16-head block) for a problem size (depends on the SM count).
 int decode_num_splits(int B, int H, int max_pages, int P, int num_sms);
 int decode_num_protected(int B, int H, int max_pages, int P, int S, int W, int num_sms);
+// Workspace layout of a decode call: kArriveBytes of merge counters (zero between calls), then the
+// partial outputs and the partial maxima and sums.
+constexpr size_t kArriveBytes = 8192;
+constexpr int kMaxArriveGroups = static_cast<int>(kArriveBytes / 8);
 size_t decode_workspace_bytes(int B, int H, int n_slots);  // n_slots = n_split + n_q
 int decode_share_slots(int B, int H, int max_pages, int P, int n_split, int n_q, int num_sms);
 // Head counts that are multiples of 64 run the packed shares on tcgen05 tensor cores (64 heads
@@ -136,6 +144,9 @@ inline bool decode_uses_tc(int H) { return H % 64 == 0; }
 int decode_tc_num_splits(int B, int H, int max_pages, int P, int num_sms);
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+// Kernel launches of one decode call on the current device (1: partials merged in place; 2: a
+// merge launch follows; 3: 64-head blocks), or -1 on a CUDA error.
+int decode_launch_count(int bits_c, int B, int H, int n_split, int n_q, int share_slots);
 // Unquantized comparator: decode over a paged BF16 cache [n_pages][P][576] (every share BF16).
 int decode_bf16_num_parts(int B, int H, int max_pages, int P, int num_sms);
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t stream);

@@ -233,7 +233,8 @@ int mla_qcache_decode_attn_pending(const mla_qcache_config* cfg, int32_t B, int3
  *   H          heads per position, a multiple of 16; q_len * H <= 256; q_len - 1 <= W.
  *   q_lat      [B][q_len][H][512] BF16, q_rope [B][q_len][H][64] BF16 (position-major rows);
  *   out, lse   [B][q_len][H][512] float32, [B][q_len][H] float32.
- *   workspace  mla_qcache_workspace_bytes(cfg, B, q_len * H, max_pages) bytes.
+ *   workspace  mla_qcache_workspace_bytes(cfg, B, q_len * H, max_pages) bytes (first 8192
+ *              bytes zero, as for mla_qcache_decode_attn).
  * Other arguments and errors as mla_qcache_decode_attn (with q_len * H rows); bad q_len ->
  * MLA_QCACHE_ERR_SHAPE. q_len = 1 is mla_qcache_decode_attn. At q_len * H a multiple of 64 the
  * packed pages are read once for all positions (64 rows per tensor-memory CTA).
@@ -252,7 +253,8 @@ int mla_qcache_decode_attn_multi(const mla_qcache_config* cfg, int32_t B, int32_
  *   kv_pool    [n_pages][page_size][576] BF16 (c then k_R per token), 16-byte aligned; token
  *              t of sequence b lives in row t % page_size of page page_table[b][t / page_size].
  *   page_size  32, 64 or 128. Other arguments as mla_qcache_decode_attn (no sink/recent
- *              buffers, no quantization config); workspace of mla_qcache_bf16_workspace_bytes.
+ *              buffers, no quantization config); workspace of mla_qcache_bf16_workspace_bytes
+ *              (first 8192 bytes zero, as for mla_qcache_decode_attn).
  * Errors: as mla_qcache_decode_attn; a bad page id sets MLA_QCACHE_DEV_BAD_PAGE and drops the
  * share that would read it.
  */
@@ -339,6 +341,16 @@ int mla_qcache_decode_plan(const mla_qcache_config* cfg, int32_t B, int32_t H, i
                            int32_t* plan);
 
 /*
+ * Kernel launches one mla_qcache_decode_attn call of this shape makes on the current device:
+ * 1 (the partials merged inside the decode launch), 2 (a merge launch follows) or 3 (64-head
+ * blocks: protected shares, tensor-memory shares, merge). For sizing CUDA graphs and counting
+ * launches; the first call sets the kernels' shared-memory attribute, as a first decode call
+ * does. Returns the count, or a negative status: bad config -> MLA_QCACHE_ERR_CONFIG/NULL; bad
+ * sizes -> MLA_QCACHE_ERR_SHAPE; a failed runtime query -> MLA_QCACHE_ERR_CUDA.
+ */
+int mla_qcache_decode_launches(const mla_qcache_config* cfg, int32_t B, int32_t H, int32_t max_pages);
+
+/*
  * Query absorption (RAQ-MLA page, Figure 4: the decode scores the latent directly, so the
  * query's no-position part is carried into the latent space through W_UK, with A_c^-1 folded
  * into W_UK offline; k_R's transform is compensated on the query side):
@@ -409,8 +421,19 @@ int mla_qcache_advance(const int32_t* cu_new, int32_t* seq_lens, int32_t B, void
  *   pool, sink_buf, recent_buf as written by mla_qcache_write.
  *   out        [B][H][512] float32, lse [B][H] float32.
  *   workspace  device scratch of at least mla_qcache_workspace_bytes(cfg, B, H, max_pages)
- *              bytes, 256-byte aligned; it needs no initialization and its contents are
- *              meaningless after the call. Calls sharing one workspace must not overlap.
+ *              bytes, 256-byte aligned. Its first 8192 bytes are the split merge's arrival
+ *              counters: zero them once before the first call on this workspace (for example
+ *              cudaMemset after allocating it); every call leaves them zero, whatever its
+ *              shape, so one workspace serves calls of any size. The rest is scratch whose
+ *              contents are meaningless after the call. Calls sharing one workspace must not
+ *              overlap. Counters that are not zero make the call report
+ *              MLA_QCACHE_DEV_TIMEOUT (the merge of a sequence whose shares see an invalid
+ *              count is abandoned, at the latest after the bounded wait) and may stay invalid:
+ *              after that bit, zero the first 8192 bytes again.
+ * How the partials are merged: when the call's CTAs fit on the GPU at once (one wave) and each
+ * (sequence, 16-head block) has many partials (24 or more), its CTAs merge their own partials at
+ * the end of the decode launch (a cooperative launch: every CTA is resident); otherwise a
+ * second launch merges them (mla_qcache_decode_launches tells which).
  * Errors: as for the writer, plus H not a multiple of 16 or > 256, workspace too small.
  */
 int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H,
@@ -441,9 +464,10 @@ int mla_qcache_decode_attn(const mla_qcache_config* cfg, int32_t B, int32_t H,
  * threads may make their first calls concurrently (the cache is atomic). cudaDeviceReset
  * reloads the library's device code, after which the cached address is stale: a process that
  * resets a device must not call this entry point on it again. Every
- * call shares the one array and leaves its contents behind; nothing in it needs to start at
- * zero because each call writes every partial result it later reads. Calls that overlap on the
- * GPU (two streams, or two host threads) race on the scratch: serialize them.
+ * call shares the one array. Its first 8192 bytes are the merge counters described under
+ * mla_qcache_decode_attn: zero when the library is loaded, left zero by every call; the rest
+ * needs no initial value (each call writes every partial result it later reads). Calls that
+ * overlap on the GPU (two streams, or two host threads) race on the scratch: serialize them.
  */
 int mla_qcache_decode_attn_noalloc(const mla_qcache_config* cfg, int32_t B, int32_t H,
                                    const uint16_t* q_lat, const uint16_t* q_rope,

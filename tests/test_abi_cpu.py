@@ -216,6 +216,9 @@ def test_decode_plan_shapes(L):
         assert parts <= 8 * per_wave and (parts <= per_wave or parts % per_wave == 0)
     # errors
     assert L.lib().mla_qcache_decode_plan(ctypes.byref(c4), 1, 24, 10, sms, (ctypes.c_int32 * 5)()) == -3
+    assert L.lib().mla_qcache_decode_launches(ctypes.byref(c4), 1, 24, 10) == -3
+    assert L.lib().mla_qcache_decode_launches(ctypes.byref(c4), 0, 16, 10) == -3
+    assert L.lib().mla_qcache_decode_launches(None, 1, 16, 10) == -1
     assert L.lib().mla_qcache_decode_plan(ctypes.byref(c4), 1, 16, 10, sms, None) == -1
 
 

@@ -37,7 +37,7 @@ def _run(lens, P, heads, seed=3, scale=0.072, bad_page=None):
     d_pt, d_pool = gu.dev(pt), gu.dev(pool.view(np.int16))
     out = torch.empty((B, H, 512), dtype=torch.float32, device="cuda")
     lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
-    ws = torch.empty(q.bf16_workspace_bytes(B, H, pt.shape[1], P), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(q.bf16_workspace_bytes(B, H, pt.shape[1], P), dtype=torch.uint8, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     q.mla_qcache_decode_attn_bf16(gu.dev(inp.q_lat), gu.dev(inp.q_rope), d_pt, P, gu.dev(inp.seq_lens), d_pool,
                                   scale, out, lse, ws, err)

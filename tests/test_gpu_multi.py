@@ -25,7 +25,7 @@ def _run(w, lens, heads, q_len, scale=None):
     ql, qr = workloads.draw_queries(np.random.default_rng(int(lens.sum()) + q_len), B, R)
     out = torch.empty((B, R, 512), dtype=torch.float32, device="cuda")
     lse = torch.empty((B, R), dtype=torch.float32, device="cuda")
-    ws = torch.empty(max(16, q.workspace_bytes(cache.cfg, B, R, inp.page_table.shape[1])), dtype=torch.uint8,
+    ws = torch.zeros(max(16, q.workspace_bytes(cache.cfg, B, R, inp.page_table.shape[1])), dtype=torch.uint8,
                      device="cuda")
     sc = w.softmax_scale if scale is None else scale
     q.mla_qcache_decode_attn_multi(cache.cfg, q_len, gu.dev(ql), gu.dev(qr), cache.page_table, cache.seq_lens,

@@ -51,7 +51,7 @@ def test_pending_decode_with_concurrent_writer(bits_c, P, S, W, heads, steps):
     cu1 = torch.arange(B + 1, dtype=torch.int32, device="cuda")
     lens_next = torch.empty_like(cache.seq_lens)
     ws = cache.workspace(heads)
-    ws2 = torch.empty_like(ws)
+    ws2 = torch.zeros_like(ws)
     out = torch.empty((B, heads, 512), dtype=torch.float32, device="cuda")
     lse = torch.empty((B, heads), dtype=torch.float32, device="cuda")
     side = torch.cuda.Stream()
