@@ -413,7 +413,8 @@ def measure_workload(args, w, q, dev, steps, warmup, layers, with_e2e):
     cfg = q.make_config(**w.config_kwargs())
     B, H = w.batch, w.heads
 
-    steps_total = warmup + steps + 8
+    # tokens one layer may gain: warm-up, the timed graph replayed twice (warm, timed), the e2e graph twice
+    steps_total = warmup + 3 * steps + 40
     inp = workloads.make_inputs(w, extra_pages=math.ceil(steps_total / w.page_size) + 1)
     max_pages = inp.page_table.shape[1]
     per_layer = inp.n_pages * q.page_bytes(cfg)
@@ -463,13 +464,23 @@ def measure_workload(args, w, q, dev, steps, warmup, layers, with_e2e):
 
     write_stream = torch.cuda.Stream(device=dev)
 
-    # Two CUDA graphs per layer (write + decode, lengths A -> B and B -> A) replayed alternately:
-    # the timed region replays exactly K of them. Inside a step the writer (with the length
-    # update) runs on a forked stream concurrently with the decode of the pending rows, joined
-    # before the step ends (the next step's decode reads what this step wrote). A second live
-    # pass replays decode-only graphs with CUDA events around each call to measure the decode
-    # kernels for the roofline.
-    g_step, g_dec = [], []
+    def step_body(cache, lens_in, lens_out):
+        # the writer forks from the step's start; the decode's node is created first (measured:
+        # the writer then delays the decode's one wave of CTAs less); joined before the step ends
+        # (the next step's decode reads what this step wrote)
+        ev_fork = torch.cuda.Event()
+        ev_fork.record(stream)
+        pending_step(cache, lens_in)
+        write_stream.wait_event(ev_fork)
+        with torch.cuda.stream(write_stream):
+            write_step(cache, lens_in, lens_out)
+        stream.wait_stream(write_stream)
+
+    # Warm-up: two CUDA graphs per layer (write + decode, lengths A -> B and B -> A) replayed
+    # alternately. Timed: the K steps, rotating over the layers as a decode iteration over K
+    # layers would, captured as one CUDA graph and replayed once (after one untimed replay); the
+    # decode-only calls of the roofline likewise, K of them in one graph.
+    g_step = []
     with torch.cuda.stream(stream):
         for cache in caches:  # warm the code paths once before capture
             decode_step(cache, cache.seq_lens)
@@ -479,21 +490,9 @@ def measure_workload(args, w, q, dev, steps, warmup, layers, with_e2e):
             for lens_in, lens_out in ((cache.seq_lens, alt), (alt, cache.seq_lens)):
                 gs = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(gs, stream=stream):
-                    # the writer forks from the step's start; the decode's node is created first
-                    # (measured: the writer then delays the decode's one wave of CTAs less)
-                    ev_fork = torch.cuda.Event()
-                    ev_fork.record(stream)
-                    pending_step(cache, lens_in)
-                    write_stream.wait_event(ev_fork)
-                    with torch.cuda.stream(write_stream):
-                        write_step(cache, lens_in, lens_out)
-                    stream.wait_stream(write_stream)
+                    step_body(cache, lens_in, lens_out)
                 pair.append(gs)
-            gd = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gd, stream=stream):
-                decode_step(cache, cache.seq_lens)
             g_step.append(pair)
-            g_dec.append(gd)
     torch.cuda.synchronize()
     uses = [0] * NL
 
@@ -502,11 +501,42 @@ def measure_workload(args, w, q, dev, steps, warmup, layers, with_e2e):
         g_step[layer][uses[layer] & 1].replay()
         uses[layer] += 1
 
+    def capture_steps(k0):
+        # K consecutive steps from step k0 on, each layer's length arrays in the roles its use
+        # count gives (the count advances as the graph is replayed, see run_timed)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream), torch.cuda.graph(g, stream=stream):
+            u = list(uses)
+            for k in range(steps):
+                layer = (k0 + k) % NL
+                cache, alt = caches[layer], lens_alt[layer]
+                lens_in, lens_out = (cache.seq_lens, alt) if u[layer] % 2 == 0 else (alt, cache.seq_lens)
+                u[layer] += 1
+                step_body(cache, lens_in, lens_out)
+        return g
+
+    def advance_uses(k0):
+        for k in range(steps):
+            uses[(k0 + k) % NL] += 1
+
     head_start = torch.empty(int(1.5e9) // 4, dtype=torch.float32, device=dev)  # lets the host queue ahead
 
     with torch.cuda.stream(stream):
         for k in range(warmup):
             replay_step(k)
+        torch.cuda.synchronize()
+        g_warm = capture_steps(warmup)  # the same K steps once untimed (graph upload, clocks)
+        g_warm.replay()
+        advance_uses(warmup)
+        torch.cuda.synchronize()
+        del g_warm
+        k0 = warmup + steps
+        g_timed = capture_steps(k0)
+        g_dec = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_dec, stream=stream):
+            for k in range(steps):
+                cache = caches[(k0 + k) % NL]
+                decode_step(cache, cache.seq_lens)
         torch.cuda.synchronize()
         if ws > 1:
             torch.distributed.barrier()
@@ -514,20 +544,21 @@ def measure_workload(args, w, q, dev, steps, warmup, layers, with_e2e):
         with ClockSampler(local) as clk:
             head_start.fill_(1.0)
             start.record(stream)
-            for k in range(steps):
-                replay_step(warmup + k)
+            g_timed.replay()
             end.record(stream)
             torch.cuda.synchronize()
+        advance_uses(k0)
         total_ms = start.elapsed_time(end)
-        # decode-only pass (same caches, lengths unchanged): per-call device time
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        head_start.fill_(2.0)
-        for k in range(steps):
-            ev[k][0].record(stream)
-            g_dec[k % NL].replay()
-            ev[k][1].record(stream)
+        # decode-only pass (same caches, lengths unchanged): K calls in one graph, once warm
+        g_dec.replay()
         torch.cuda.synchronize()
-        dec_ms = [a.elapsed_time(b) for a, b in ev]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        head_start.fill_(2.0)
+        a.record(stream)
+        g_dec.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        dec_ms = [a.elapsed_time(b) / steps]
     if ws > 1:
         total_ms = max_over_ranks(total_ms, dev)
     if any(c.error_bits() for c in caches):
