@@ -68,7 +68,15 @@ struct Geom {
 
 constexpr int kXsFloats = 2 * 4 * 16 * kXStride;  // partial scores [2 buf][4 warps][16 heads][32 tok]
 constexpr int kXpFloats = 2 * 16 * kXStride;      // weights [2 buf][16 heads][32 tok]
-constexpr int kNumBars = 12;                       // >= stages + 4 exchange barriers
+constexpr int kNumBars = 12;                       // >= stages + 4 exchange barriers + query barrier
+// Packed CTAs fetch the 16 query rows of their head block with bulk copies into the (still idle)
+// partial-score buffer: latent rows padded to kQRowBytes (each 8-lane phase of the prologue's
+// 16-byte reads covers 32 distinct banks), then the 16 k_R rows; completion on barrier kQueryBar.
+constexpr int kQRowBytes = kLatent * 2 + 64;
+constexpr int kQRopeOff = 16 * kQRowBytes;
+constexpr int kQBytes = 16 * kLatent * 2 + 16 * kRope * 2;  // bytes the copies deliver
+constexpr int kQueryBar = 8;
+static_assert(kQRopeOff + 16 * kRope * 2 <= kXsFloats * 4, "query rows fit the partial-score buffer");
 
 template <int BITS>
 __host__ __device__ constexpr int smem_bytes() {
@@ -78,7 +86,7 @@ __host__ __device__ constexpr int smem_bytes() {
 // kCtasPerSm CTAs (each with 1 KB reserved by the hardware) fit in an SM's 228 KB
 static_assert(kCtasPerSm * (smem_bytes<4>() + 1024) <= 228 * 1024 &&
                   kCtasPerSm * (smem_bytes<2>() + 1024) <= 228 * 1024, "shared memory per SM");
-static_assert(Geom<4>::kStages + 4 <= kNumBars && Geom<2>::kStages + 4 <= kNumBars, "barriers");
+static_assert(Geom<4>::kStages + 4 <= kQueryBar && Geom<2>::kStages + 4 <= kQueryBar && kQueryBar < kNumBars, "barriers");
 template <int BITS>
 constexpr int xflags_offset() {
   return Geom<BITS>::kRegion + (kXsFloats + kXpFloats + 2 * 16 + 4 * 16) * 4 + kNumBars * 8;
@@ -438,9 +446,83 @@ __host__ __device__ constexpr int out_log2w(int cb) {
   return BITS == 4 ? 4 * (cb & 1) : 2 * ((cb & 7) <= 4 ? (cb & 7) : (cb & 7) - 5);
 }
 
+// The same rows for a query that is not 16-byte aligned, element by element by every thread (kept
+// out of line: the rare path does not weigh on the kernel's register allocation).
+__device__ __noinline__ void copy_query(const DecodeParams& p, const Shared& sh, int b, int h0) {
+  uint16_t* rows = reinterpret_cast<uint16_t*>(sh.sbuf);
+  const uint16_t* ql = p.q_lat + (static_cast<size_t>(b) * p.H + h0) * kLatent;
+  const uint16_t* qk = p.q_rope + (static_cast<size_t>(b) * p.H + h0) * kRope;
+  for (int e = threadIdx.x; e < 16 * kLatent; e += kThreads)
+    rows[(e / kLatent) * (kQRowBytes / 2) + e % kLatent] = __ldg(ql + e);
+  for (int e = threadIdx.x; e < 16 * kRope; e += kThreads) rows[kQRopeOff / 2 + e] = __ldg(qk + e);
+}
+
+// The prologue's BF16 query words from the bulk-copied rows: lane (g, q) of warp w gets the pairs
+// of channels slot_channel(kc, 2j, q), slot_channel(kc, 2j + 1, q) of rows g (qa[kc][2j]) and
+// g + 8 (qa[kc][2j + 1]) from one 16-byte read per row and channel octet (INT4: the octet
+// 32m + 8q .. + 7 serves k-chunks 2m and 2m + 1; INT2: two octets 64m + 16q .. + 15 serve
+// k-chunks 4m .. 4m + 3), and the k_R words of rows g, g + 8 at dims 16w + 2q and 16w + 2q + 8.
+template <int BITS>
+__device__ __forceinline__ void load_query_smem(const uint8_t* rows, int warp, int g, int q, uint32_t (&qa)[8][4],
+                                                uint32_t (&qrw)[4]) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const uint8_t* row = rows + (g + 8 * r) * kQRowBytes + 2 * 128 * warp;
+    if constexpr (BITS == 4) {
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + 2 * (32 * m + 8 * q));
+        qa[2 * m][r] = __byte_perm(v.x, v.z, 0x5410);          // channels +0, +4
+        qa[2 * m][2 + r] = __byte_perm(v.y, v.w, 0x5410);      // +2, +6
+        qa[2 * m + 1][r] = __byte_perm(v.x, v.z, 0x7632);      // +1, +5
+        qa[2 * m + 1][2 + r] = __byte_perm(v.y, v.w, 0x7632);  // +3, +7
+      }
+    } else {
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const uint4 a = *reinterpret_cast<const uint4*>(row + 2 * (64 * m + 16 * q));
+        const uint4 c = *reinterpret_cast<const uint4*>(row + 2 * (64 * m + 16 * q + 8));
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          qa[4 * m + t][r] = __byte_perm(aw[t], cw[t], 0x5410);      // channels 2t, 8 + 2t
+          qa[4 * m + t][2 + r] = __byte_perm(aw[t], cw[t], 0x7632);  // 2t + 1, 9 + 2t
+        }
+      }
+    }
+  }
+  const uint8_t* kr = rows + kQRopeOff + g * (kRope * 2) + 2 * (16 * warp + 2 * q);
+  qrw[0] = *reinterpret_cast<const uint32_t*>(kr);
+  qrw[1] = *reinterpret_cast<const uint32_t*>(kr + 8 * kRope * 2);
+  qrw[2] = *reinterpret_cast<const uint32_t*>(kr + 16);
+  qrw[3] = *reinterpret_cast<const uint32_t*>(kr + 8 * kRope * 2 + 16);
+}
+
+// Packed CTAs bulk-copy the query when both query pointers are 16-byte aligned.
+__device__ __forceinline__ bool query_bulk(const DecodeParams& p) {
+  return ((reinterpret_cast<uintptr_t>(p.q_lat) | reinterpret_cast<uintptr_t>(p.q_rope)) & 15u) == 0;
+}
+
+// Thread 0 of a packed CTA, first thing in the kernel: the head block's 16 latent query rows and
+// 16 k_R query rows into the partial-score buffer by bulk copies (one per latent row, one for the
+// k_R rows), so that their round trip overlaps the sequence-length and page-table reads. Needs
+// 16-byte aligned query pointers (the rows of a block are then aligned too).
+__device__ __forceinline__ void fetch_query(const DecodeParams& p, const Shared& sh, int b, int h0) {
+  uint64_t* bar = sh.bars + kQueryBar;
+  mbar_init(bar, 1);
+  fence_mbar_init();
+  fence_proxy_async_smem();
+  mbar_arrive_expect_tx(bar, kQBytes);
+  uint8_t* dst = reinterpret_cast<uint8_t*>(sh.sbuf);
+  const uint16_t* src = p.q_lat + (static_cast<size_t>(b) * p.H + h0) * kLatent;
+  for (int r = 0; r < 16; ++r) bulk_g2s(dst + r * kQRowBytes, src + r * kLatent, kLatent * 2, bar);
+  bulk_g2s(dst + kQRopeOff, p.q_rope + (static_cast<size_t>(b) * p.H + h0) * kRope, 16 * kRope * 2, bar);
+}
+
 template <int BITS, bool kBalanced>
 __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int T, int split, State& st,
                              int32_t& flags) {
+  const bool q_bulk = query_bulk(p);
   using G = Geom<BITS>;
   constexpr int kS = G::kStages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
@@ -490,7 +572,10 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
       n_my = tile_end - tile_begin;
     }
   }
-  if (n_my == 0) return;  // empty share (a short sequence): the merge sees sum 0 and skips it
+  if (n_my == 0) {  // empty share (a short sequence): the merge sees sum 0 and skips it
+    if (q_bulk && !mbar_wait_bounded(sh.bars + kQueryBar, 0, kWaitBudget)) flags |= kErrTimeout;  // copies landed
+    return;
+  }
   const int pg0 = (tile_begin * kPT) >> p.p_shift;
   // validate the page ids this split reads; a bad id drops the split's work
   {
@@ -528,21 +613,26 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
   int issued = n_my < kS ? n_my : kS;  // identical in every thread
 
   // ---- query operands: FP16 with a per-head power-of-two prescale, in the masks' channel order
-  uint32_t qa[8][4];
+  // (BF16 words first, from the rows in the partial-score buffer, which the kernel's start
+  // bulk-copies there or, for a query that is not 16-byte aligned, stores element by element;
+  // qrw: the k_R slice, rows g, g+8, dims 16w + {2q, 2q+1} and 16w + {2q+8, 2q+9})
+  uint32_t qa[8][4], qrw[4];
+  if (q_bulk) {
+    if (!mbar_wait_bounded(sh.bars + kQueryBar, 0, kWaitBudget)) {
+      flags |= kErrTimeout;
+      (void)mbar_wait_bounded(sh.bars + kQueryBar, 0, kWaitBudget >> 4);
+    }
+  }
+  load_query_smem<BITS>(reinterpret_cast<const uint8_t*>(sh.sbuf), warp, g, q, qa, qrw);
   float qsum[2] = {0.f, 0.f}, inv_f[2], head_scale;  // inv_f: prologue only
   {
-    const uint16_t* r0 = p.q_lat + (static_cast<size_t>(b) * p.H + h0 + g) * kLatent + 128 * warp;
-    const uint16_t* r1 = r0 + 8 * kLatent;
     float mx0 = 0.f, mx1 = 0.f;
 #pragma unroll
     for (int kc = 0; kc < 8; ++kc)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int c0 = slot_channel<BITS>(kc, 2 * j, q), c1 = slot_channel<BITS>(kc, 2 * j + 1, q);
-        const uint32_t v0 = static_cast<uint32_t>(__ldg(r0 + c0)) | (static_cast<uint32_t>(__ldg(r0 + c1)) << 16);
-        const uint32_t v1 = static_cast<uint32_t>(__ldg(r1 + c0)) | (static_cast<uint32_t>(__ldg(r1 + c1)) << 16);
-        qa[kc][2 * j] = v0;      // a0 / a2: row g
-        qa[kc][2 * j + 1] = v1;  // a1 / a3: row g + 8
+        const uint32_t v0 = qa[kc][2 * j];      // a0 / a2: row g
+        const uint32_t v1 = qa[kc][2 * j + 1];  // a1 / a3: row g + 8
         qsum[0] += bf16_lo(v0) + bf16_hi(v0);
         qsum[1] += bf16_lo(v1) + bf16_hi(v1);
         mx0 = fmaxf(mx0, fmaxf(fabsf(bf16_lo(v0)), fabsf(bf16_hi(v0))));
@@ -596,9 +686,7 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
   // k_R query slice: rows g, g+8, dims 16w + {2q, 2q+1, 2q+8, 2q+9}, kept in shared memory
   {
     float qr[8];
-    const uint32_t* r0 = reinterpret_cast<const uint32_t*>(p.q_rope + (static_cast<size_t>(b) * p.H + h0 + g) * kRope + 16 * warp);
-    const uint32_t* r1 = r0 + 8 * kRope / 2;
-    const uint32_t u0 = __ldg(r0 + q), u1 = __ldg(r1 + q), u2 = __ldg(r0 + 4 + q), u3 = __ldg(r1 + 4 + q);
+    const uint32_t u0 = qrw[0], u1 = qrw[1], u2 = qrw[2], u3 = qrw[3];
     qr[0] = bf16_lo(u0);
     qr[1] = bf16_hi(u0);
     qr[2] = bf16_lo(u2);
@@ -1162,6 +1250,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h0 = blockIdx.y * 16;
   int32_t flags = 0;
+  if (is_bf16) {
+  } else if (query_bulk(p)) {
+    if (threadIdx.x == 0) fetch_query(p, sh, b, h0);
+  } else {
+    copy_query(p, sh, b, h0);  // (visible to every thread after the barrier below)
+  }
 
   int T_old;
   const int T = decode_seq_len(p, b, T_old, flags);

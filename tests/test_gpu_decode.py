@@ -102,6 +102,37 @@ def test_full_size_v2lite_decode():
     print(f"full-size rel {rel:.2e} dlse {dl:.2e}")
 
 
+@pytest.mark.parametrize("w,heads", [(C4, 16), (C4, 32), (C2, 16)])
+def test_query_alignment_does_not_change_the_result(w, heads):
+    """A query that is 4-byte but not 16-byte aligned takes the element-by-element copy instead
+    of the bulk copies: the same result, bit for bit, and within tolerance of the oracle."""
+    lens = [1000, 333, 140]
+    inp = workloads.make_inputs(w, seq_lens=np.array(lens, np.int32), heads=heads)
+    kw = w.config_kwargs()
+    cache = gu.gpu_cache(kw, inp)
+    gu.write_rows(cache, inp.c, inp.kr, inp.seq_lens, max(lens))
+    q_lat, q_rope = gu.dev(inp.q_lat), gu.dev(inp.q_rope)
+    out_a, lse_a = cache.decode(q_lat, q_rope, w.softmax_scale)
+    # the same values at a 4-byte offset inside larger buffers
+    bl = torch.empty(q_lat.numel() + 2, dtype=q_lat.dtype, device=q_lat.device)
+    br = torch.empty(q_rope.numel() + 2, dtype=q_rope.dtype, device=q_rope.device)
+    bl[2:].copy_(q_lat.reshape(-1))
+    br[2:].copy_(q_rope.reshape(-1))
+    ql_u, qr_u = bl[2:].view(q_lat.shape), br[2:].view(q_rope.shape)
+    assert ql_u.data_ptr() % 16 != 0 and qr_u.data_ptr() % 16 != 0
+    out_u, lse_u = cache.decode(ql_u, qr_u, w.softmax_scale)
+    torch.cuda.synchronize()
+    assert cache.error_bits() == 0
+    assert torch.equal(out_a, out_u) and torch.equal(lse_a, lse_u)
+    cfg, pool, sink, ring = gu.oracle_cache(kw, inp)
+    assert oracle.write(cfg, inp.c, inp.kr, inp.cu, np.zeros(len(lens), np.int32), max(lens), inp.page_table,
+                        pool, sink, ring) == 0
+    o_ref, l_ref, fl = oracle.decode(cfg, inp.q_lat, inp.q_rope, inp.page_table, inp.seq_lens, pool, sink, ring,
+                                     w.softmax_scale)
+    assert fl == 0
+    gu.check_decode(out_u, lse_u, o_ref, l_ref, TOL)
+
+
 def test_bad_page_sets_error_bit():
     inp = workloads.make_inputs(C4, seq_lens=np.array([700], np.int32))
     kw = C4.config_kwargs()
