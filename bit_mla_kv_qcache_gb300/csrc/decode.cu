@@ -1132,12 +1132,14 @@ __device__ __forceinline__ bool group_arrive(unsigned long long* ctr, int NS) {
 // columns [z*2048/n_ctas, (z+1)*2048/n_ctas) of the block's output (16 heads x 128 columns). The slice of every
 // partial and the partial maxima and sums of the slice's heads are first copied into shared
 // memory, all requests in flight at once (16-byte asynchronous copies through L2: the partials
-// were stored by other SMs during this launch). One warp per head then forms the head's
+// were stored by other SMs during this launch), the maxima and sums as a group of their own. Once
+// that group has landed (the slices still in flight), one warp per head forms the head's
 // maximum M and sum L = sum_s 2^(m_s - M) l_s and turns each partial's (m_s, l_s) into its weight
 // 2^(m_s - M) / L (and writes the head's log-sum-exp if the slice holds its first column); R
 // lanes take one column (R a power of two, as many as fill the CTA), each summing every R-th
 // weighted partial, and shuffles add the R sums. Partials of empty shares (maximum -inf) have
-// weight 0 and are selected out, never multiplied: their rows hold whatever the buffer held.
+// weight 0 and their products are dropped by selection, never added: their rows hold whatever
+// the buffer held.
 // `buf` holds merge_buf_need(NS, n_ctas) bytes (checked on the host): NS partial slots merged by
 // the group's n_ctas CTAs.
 __host__ __device__ constexpr int merge_buf_need(int NS, int n_ctas) {
@@ -1162,6 +1164,7 @@ __device__ __forceinline__ void group_merge(const DecodeParams& p, uint8_t* buf,
   float2* mls = reinterpret_cast<float2*>(buf + (ml0 & 3) * 4);  // [n_h][NS]: (m_s, l_s), then (weight, -)
   float4* os = reinterpret_cast<float4*>(buf + n_ml16 * 16);      // [NS][n_cols]
   for (int j = threadIdx.x; j < n_ml16; j += kThreads) cp_async_cg16(buf + j * 16, mlg + 4 * j);
+  cp_async_commit();  // the maxima and sums: waited for first, the weights overlap the slices' copies
   // thread -> (column, every k-th partial): k = 1 when the columns alone fill the CTA
   const int k = n_cols >= kThreads ? 1 : kThreads / n_cols;
   const int s_first = n_cols >= kThreads ? 0 : static_cast<int>(threadIdx.x) / n_cols;
@@ -1171,7 +1174,8 @@ __device__ __forceinline__ void group_merge(const DecodeParams& p, uint8_t* buf,
       const float* src = p.o_part + (bh0 + (c >> 7)) * NS * kLatent + 4 * (c & 127);
       for (int s = s_first; s < NS; s += k) cp_async_cg16(os + s * n_cols + ci, src + static_cast<size_t>(s) * kLatent);
     }
-  cp_async_wait_all();
+  cp_async_commit();
+  cp_async_wait_group<1>();
   __syncthreads();
   // per-head weights (warp w: heads w, w+4, ...)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1193,6 +1197,7 @@ __device__ __forceinline__ void group_merge(const DecodeParams& p, uint8_t* buf,
     if (lane == 0 && ((hA + hh) << 7) >= c0)  // the slice holds the head's first column
       p.lse[bh0 + hA + hh] = any ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
   }
+  cp_async_wait_group<0>();
   __syncthreads();
 
   int lg = 0;  // R = 2^lg lanes per column
@@ -1207,15 +1212,14 @@ __device__ __forceinline__ void group_merge(const DecodeParams& p, uint8_t* buf,
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (active) {
       const float2* wrow = mls + ((c >> 7) - hA) * NS;
+      // (every slot's row is loaded, so the loads of several slots are in flight together; an
+      // empty share's sums are dropped by selection: its row may hold anything)
 #pragma unroll 4
       for (int s = r; s < NS; s += R) {
         const float w = wrow[s].x;
-        if (w == 0.f) continue;
         const float4 v = os[s * n_cols + ci];
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+        const float4 t = make_float4(fmaf(w, v.x, acc.x), fmaf(w, v.y, acc.y), fmaf(w, v.z, acc.z), fmaf(w, v.w, acc.w));
+        if (w != 0.f) acc = t;
       }
     }
     for (int o = 1; o < R; o <<= 1) {

@@ -66,6 +66,13 @@ __device__ __forceinline__ void cp_async_cg16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// cp.async groups: close the group of this thread's copies issued so far; wait until at most N
+// of its groups are still in flight
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // ---------------------------------------------------------------- bulk copies (TMA engine)
 __device__ __forceinline__ void fence_proxy_async_smem() {
