@@ -572,19 +572,29 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
       n_my = tile_end - tile_begin;
     }
   }
+  // A table of at most kMaxSplitPages pages was copied whole into sh.pids at the kernel's start
+  // (before the length was known): ids by page index. A longer one: the split's ids from here on,
+  // by index relative to its first page.
+  const bool whole_table = p.max_pages <= kMaxSplitPages;
   if (n_my == 0) {  // empty share (a short sequence): the merge sees sum 0 and skips it
     if (q_bulk && !mbar_wait_bounded(sh.bars + kQueryBar, 0, kWaitBudget)) flags |= kErrTimeout;  // copies landed
+    if (whole_table) cp_async_wait_all();
     return;
   }
   const int pg0 = (tile_begin * kPT) >> p.p_shift;
+  const int pid_base = whole_table ? 0 : pg0;  // sh.pids[pg - pid_base] holds page pg's id
   // validate the page ids this split reads; a bad id drops the split's work
   {
     bool bad = false;
     const int pg1 = n_my > 0 ? (((tile_begin + n_my) * kPT - 1) >> p.p_shift) : pg0 - 1;
+    if (whole_table) {
+      cp_async_wait_all();
+      __syncthreads();
+    }
     for (int pg = pg0 + static_cast<int>(threadIdx.x); pg <= pg1; pg += kThreads) {
-      const int32_t pid = __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
+      const int32_t pid = whole_table ? sh.pids[pg] : __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
       bad |= pid < 0 || pid >= p.n_pages;
-      if (pg - pg0 < kMaxSplitPages) sh.pids[pg - pg0] = pid;  // the copies read ids from here
+      if (!whole_table && pg - pg0 < kMaxSplitPages) sh.pids[pg - pg0] = pid;  // the copies read ids from here
     }
     if (__syncthreads_or(bad)) {
       flags |= kErrBadPage;
@@ -596,8 +606,8 @@ __device__ void packed_split(const DecodeParams& p, const Shared& sh, int b, int
   auto issue = [&](int i) {
     const int t0 = (tile_begin + i) * kPT;
     const int pg = t0 >> p.p_shift, tp0 = t0 & (p.P - 1);
-    const int32_t pid = pg - pg0 < kMaxSplitPages ? sh.pids[pg - pg0]
-                                                 : __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
+    const int32_t pid = pg - pid_base < kMaxSplitPages ? sh.pids[pg - pid_base]
+                                                       : __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
     const uint8_t* base = p.pool + static_cast<size_t>(pid) * static_cast<size_t>(p.page_bytes);
     uint8_t* dst = sh.stages + (i % kS) * G::kStage;
     uint64_t* bar = sh.bars + (i % kS);
@@ -1254,15 +1264,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(const Deco
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h0 = blockIdx.y * 16;
   int32_t flags = 0;
-  if (is_bf16) {
-  } else if (query_bulk(p)) {
-    if (threadIdx.x == 0) fetch_query(p, sh, b, h0);
-  } else {
-    copy_query(p, sh, b, h0);  // (visible to every thread after the barrier below)
+  if (!is_bf16) {
+    if (query_bulk(p)) {
+      if (threadIdx.x == 0) fetch_query(p, sh, b, h0);
+    } else {
+      copy_query(p, sh, b, h0);  // (visible to every thread after the barrier below)
+    }
   }
-
+  const SeqLenWords len_words = decode_seq_len_load(p, b);
+  // a short page table whole into sh.pids while the length is in flight (the share, and so its
+  // pages, follow from the length): asynchronous 4-byte copies, waited for before the ids are read
+  if (!is_bf16 && p.max_pages <= kMaxSplitPages)
+    for (int pg = threadIdx.x; pg < p.max_pages; pg += kThreads)
+      cp_async_ca4(sh.pids + pg, p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
   int T_old;
-  const int T = decode_seq_len(p, b, T_old, flags);
+  const int T = decode_seq_len_check(p, len_words, T_old, flags);
   if (threadIdx.x == 0) {
     if (is_bf16) {  // two row stages, one arrival each
       mbar_init(sh.bars, 1);

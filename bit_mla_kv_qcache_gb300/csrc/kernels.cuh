@@ -107,16 +107,28 @@ struct DecodeParams {
 #ifdef __CUDACC__
 // Sequence b's length seen by a decode: the cached length plus its pending rows. Out-of-range
 // values set an error bit and count as an empty sequence; `T_old` receives the cached length
-// (the first pending token).
-__device__ __forceinline__ int decode_seq_len(const DecodeParams& p, int b, int& T_old, int32_t& flags) {
-  int T = __ldg(p.seq_lens + b);
-  int n_new = 0;
+// (the first pending token). In two steps, so that a kernel can issue other work between the
+// loads and the first use of their values.
+struct SeqLenWords {
+  int T, c0, c1;  // seq_lens[b]; cu_new[b], cu_new[b+1] (0, 0 without pending rows)
+};
+__device__ __forceinline__ SeqLenWords decode_seq_len_load(const DecodeParams& p, int b) {
+  SeqLenWords w;
+  w.T = __ldg(p.seq_lens + b);
+  w.c0 = w.c1 = 0;
   if (p.cu_new != nullptr) {
-    n_new = __ldg(p.cu_new + b + 1) - __ldg(p.cu_new + b);
-    if (n_new < 0 || n_new > p.max_new) {
-      flags |= kErrRows;
-      n_new = 0;
-    }
+    w.c0 = __ldg(p.cu_new + b);
+    w.c1 = __ldg(p.cu_new + b + 1);
+  }
+  return w;
+}
+__device__ __forceinline__ int decode_seq_len_check(const DecodeParams& p, const SeqLenWords& w, int& T_old,
+                                                    int32_t& flags) {
+  const int T = w.T;
+  int n_new = w.c1 - w.c0;
+  if (p.cu_new != nullptr && (n_new < 0 || n_new > p.max_new)) {
+    flags |= kErrRows;
+    n_new = 0;
   }
   if (T < 0 || static_cast<long long>(T) + n_new > static_cast<long long>(p.max_pages) * p.P) {
     flags |= kErrSeqOverflow;
@@ -125,6 +137,9 @@ __device__ __forceinline__ int decode_seq_len(const DecodeParams& p, int b, int&
   }
   T_old = T;
   return T + n_new;
+}
+__device__ __forceinline__ int decode_seq_len(const DecodeParams& p, int b, int& T_old, int32_t& flags) {
+  return decode_seq_len_check(p, decode_seq_len_load(p, b), T_old, flags);
 }
 #endif
 

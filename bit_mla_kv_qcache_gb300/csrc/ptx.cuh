@@ -61,6 +61,10 @@ __device__ __forceinline__ void red_add_release_gpu(unsigned long long* p, unsig
   asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// 4-byte global -> shared copy (cp.async; completion: cp_async_wait_all)
+__device__ __forceinline__ void cp_async_ca4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
 // 16-byte global -> shared copy through L2 only (cp.async; completion: cp_async_wait_all)
 __device__ __forceinline__ void cp_async_cg16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
