@@ -47,8 +47,8 @@ constexpr int kQBytes = kTcHeads * kRow * 2;      // 64 heads x 576 ch FP16: cor
 constexpr int kPOff = kQOff + kQBytes;
 constexpr int kPBytes = kTcTok * kTcHeads * 2;    // 128 tok x 64 heads FP16: core (tb, hb) at (8 tb + hb) * 128
 constexpr int kMiscOff = kPOff + kPBytes;
-constexpr int kBarOff = kMiscOff;                 // [0] scores done, [1] readout done
-constexpr int kTmemSlotOff = kMiscOff + 16;
+constexpr int kBarOff = kMiscOff;                 // [0] scores done, [1] readout done, [2] query rows
+constexpr int kTmemSlotOff = kMiscOff + 32;
 constexpr int kMOff = kMiscOff + 64;              // running max per head (log2 units)
 constexpr int kHsOff = kMOff + 256;               // MMA score -> log2 units, per head
 constexpr int kRedOff = kHsOff + 256;             // [4 lane quarters][64 heads] floats
@@ -59,6 +59,12 @@ constexpr int kPidOff = kTmOff + 2048;           // page ids of the share (first
 constexpr int kPidCache = 256;
 constexpr int kTcSmem = kPidOff + 4 * kPidCache;
 static_assert(kTcSmem <= 227 * 1024, "one CTA per SM");
+// The BF16 query rows of the head block, staged in the tile region before the first tile: latent
+// rows padded to kQRowWords 32-bit words (the prologue's reads fall in distinct banks), then the
+// k_R rows.
+constexpr int kQRowWords = kLatent / 2 + 4;
+constexpr int kQRopeStage = kTcHeads * kQRowWords * 4;
+static_assert(kQRopeStage + kTcHeads * kRope * 2 <= kTileBytes && (kQRowWords * 4) % 16 == 0, "query staging");
 static_assert(kTileOff % 1024 == 0 && kQOff % 1024 == 0 && kPOff % 1024 == 0, "operand alignment");
 
 // tensor memory columns (512 allocated; FP32 accumulators, lane = row)
@@ -240,6 +246,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
   const int NS = p.n_split + p.n_q;
   int32_t flags = 0;
 
+  // The head block's query rows into the (still unused) tile region by bulk copies, first thing:
+  // their round trip overlaps the length and page-table reads (16-byte aligned query pointers;
+  // else they are read element by element below).
+  const bool q_bulk = ((reinterpret_cast<uintptr_t>(p.q_lat) | reinterpret_cast<uintptr_t>(p.q_rope)) & 15u) == 0;
+  uint32_t* const qlat_s = reinterpret_cast<uint32_t*>(smem + kTileOff);
+  uint32_t* const qrope_s = reinterpret_cast<uint32_t*>(smem + kTileOff + kQRopeStage);
+  if (q_bulk) {
+    if (tid == 0) {
+      mbar_init(bars + 2, 1);
+      fence_mbar_init();
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bars + 2, kTcHeads * (kLatent + kRope) * 2);
+    }
+    __syncthreads();
+    if (tid < kTcHeads)
+      bulk_g2s(qlat_s + tid * kQRowWords, p.q_lat + (static_cast<size_t>(b) * p.H + h0 + tid) * kLatent, kLatent * 2,
+               bars + 2);
+    else if (tid == kTcHeads)
+      bulk_g2s(qrope_s, p.q_rope + (static_cast<size_t>(b) * p.H + h0) * kRope, kTcHeads * kRope * 2, bars + 2);
+  }
+
   int T_old;
   const int T = decode_seq_len(p, b, T_old, flags);
   const int lo = p.S, hi = T - p.W;
@@ -268,6 +295,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
     }
   }
   if (n_my == 0) {  // empty share: the merge sees sum 0 and skips the slot
+    if (q_bulk && !mbar_wait_bounded(bars + 2, 0, kTcWaitBudget)) flags |= kErrTimeout;  // the copies landed
     if (tid < kTcHeads) {
       float* ml = p.ml_part + ((static_cast<size_t>(b) * p.H + h0 + tid) * NS + split) * 2;
       ml[0] = -INFINITY;
@@ -291,27 +319,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
   }
 
   // ---- query: FP16, per-head power-of-two prescale 2^E, divided by the field weight of the
-  // code operand at each tile position; per-group sums for the minimum terms. The BF16 rows
-  // are first copied into the (still unused) tile region with one batch of independent loads.
+  // code operand at each tile position; per-group sums for the minimum terms. The BF16 rows are
+  // in the tile region: bulk-copied at the start, or copied here with one batch of independent
+  // loads when the query is not 16-byte aligned.
   {
-    constexpr int kWords = kRow / 2;    // 288 32-bit words per head (latent, then rope)
-    constexpr int kStride = kWords + 1;  // padded row: the four threads of a head hit distinct banks
-    uint32_t* qraw = reinterpret_cast<uint32_t*>(smem + kTileOff);
-    // the query rows are 4-byte aligned (32-bit loads)
-    const uint32_t* ql = reinterpret_cast<const uint32_t*>(p.q_lat + (static_cast<size_t>(b) * p.H + h0) * kLatent);
-    const uint32_t* qr = reinterpret_cast<const uint32_t*>(p.q_rope + (static_cast<size_t>(b) * p.H + h0) * kRope);
+    if (q_bulk) {
+      if (!mbar_wait_bounded(bars + 2, 0, kTcWaitBudget)) {
+        flags |= kErrTimeout;
+        (void)mbar_wait_bounded(bars + 2, 0, kTcWaitBudget >> 4);
+      }
+    } else {
+      // the query rows are 4-byte aligned (32-bit loads)
+      const uint32_t* ql = reinterpret_cast<const uint32_t*>(p.q_lat + (static_cast<size_t>(b) * p.H + h0) * kLatent);
+      const uint32_t* qr = reinterpret_cast<const uint32_t*>(p.q_rope + (static_cast<size_t>(b) * p.H + h0) * kRope);
 #pragma unroll 12
-    for (int it = 0; it < kTcHeads * kWords / kTcThreads; ++it) {
-      const int w = it * kTcThreads + tid, h = w / kWords, k = w - h * kWords;
-      qraw[h * kStride + k] = k < kLatent / 2 ? __ldg(ql + h * (kLatent / 2) + k) : __ldg(qr + h * (kRope / 2) + k - kLatent / 2);
+      for (int it = 0; it < kTcHeads * (kRow / 2) / kTcThreads; ++it) {
+        const int w = it * kTcThreads + tid, h = w / (kRow / 2), k = w - h * (kRow / 2);
+        if (k < kLatent / 2) qlat_s[h * kQRowWords + k] = __ldg(ql + h * (kLatent / 2) + k);
+        else qrope_s[h * (kRope / 2) + k - kLatent / 2] = __ldg(qr + h * (kRope / 2) + k - kLatent / 2);
+      }
     }
     __syncthreads();
     const int h = tid >> 2, part = tid & 3;  // 4 threads per head
-    const uint32_t* row = qraw + h * kStride;
+    const uint32_t* row = qlat_s + h * kQRowWords;
     float mx = 0.f, gs = 0.f;
 #pragma unroll 8
-    for (int k = part; k < kWords; k += 4) {
+    for (int k = part; k < kLatent / 2; k += 4) {
       const uint32_t w = row[k];
+      mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w))));
+    }
+#pragma unroll
+    for (int k = part; k < kRope / 2; k += 4) {
+      const uint32_t w = qrope_s[h * (kRope / 2) + k];
       mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w))));
     }
 #pragma unroll 8
@@ -335,13 +374,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
       const int hh = idx & (kTcHeads - 1), blk = idx >> 6;  // 16-channel block
       const int Eh = static_cast<int>(red[hh]);
       const bool lat = blk < kLatent / 16;
-      const uint32_t* src = qraw + hh * kStride + 8 * blk;
+      const uint32_t* src = lat ? qlat_s + hh * kQRowWords + 8 * blk : qrope_s + hh * (kRope / 2) + 8 * (blk - kLatent / 16);
+      const uint4 s0 = reinterpret_cast<const uint4*>(src)[0], s1 = reinterpret_cast<const uint4*>(src)[1];
+      const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
       float x[16];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const uint32_t w = src[k];
-        x[2 * k] = bf16_lo(w);
-        x[2 * k + 1] = bf16_hi(w);
+        x[2 * k] = bf16_lo(sw[k]);
+        x[2 * k + 1] = bf16_hi(sw[k]);
       }
       uint32_t o[8];
 #pragma unroll

@@ -102,10 +102,11 @@ def test_full_size_v2lite_decode():
     print(f"full-size rel {rel:.2e} dlse {dl:.2e}")
 
 
-@pytest.mark.parametrize("w,heads", [(C4, 16), (C4, 32), (C2, 16)])
+@pytest.mark.parametrize("w,heads", [(C4, 16), (C4, 32), (C2, 16), (C4, 128), (C2, 64)])
 def test_query_alignment_does_not_change_the_result(w, heads):
     """A query that is 4-byte but not 16-byte aligned takes the element-by-element copy instead
-    of the bulk copies: the same result, bit for bit, and within tolerance of the oracle."""
+    of the bulk copies (16-head blocks, and the 64-head tensor-memory kernel): the same result,
+    bit for bit, and within tolerance of the oracle."""
     lens = [1000, 333, 140]
     inp = workloads.make_inputs(w, seq_lens=np.array(lens, np.int32), heads=heads)
     kw = w.config_kwargs()
