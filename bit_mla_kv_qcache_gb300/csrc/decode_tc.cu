@@ -318,6 +318,50 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
     fence_mbar_init();
   }
 
+  // ---- per-tile packed loads (issued one tile ahead)
+  const size_t P = static_cast<size_t>(p.P);
+  auto page_base = [&](int pos) -> const uint8_t* {
+    const int pg = pos >> p.p_shift;
+    const int32_t pid = pg - pg0 < kPidCache ? pids[pg - pg0]
+                                             : __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
+    return p.pool + static_cast<size_t>(pid) * static_cast<size_t>(p.page_bytes);
+  };
+  TileRegs<BITS> R;
+  auto load_tile = [&](int i) {
+    const int t0 = (tile_begin + i) * kTcTok;
+#pragma unroll
+    for (int it = 0; it < G::kItems; ++it) {
+      const int tb = G::tb_of(warp, it), jb = G::jb_of(it);
+      const int t = 8 * tb + (lane & 7), j = 4 * jb + (lane >> 3);
+      const int pos = t0 + t;
+      R.lat[it] = make_uint4(0u, 0u, 0u, 0u);
+      if (pos < hi) {
+        const uint8_t* base = page_base(pos);
+        const int slot = pos & (p.P - 1);
+        R.lat[it] = __ldg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(slot) * G::kRowBytes +
+                                                         16 * (j ^ (slot & 7))));
+      }
+    }
+    const int pos = t0 + 32 * quarter + lane;
+    R.tmeta = R.krw[0] = R.krw[1] = make_uint4(0u, 0u, 0u, 0u);
+    if (pos < hi) {
+      const uint8_t* base = page_base(pos);
+      const int slot = pos & (p.P - 1);
+      R.tmeta = __ldg(reinterpret_cast<const uint4*>(base + P * (G::kRowBytes + 32) + slot * 16));
+      const uint8_t* regb = base + P * G::kRowBytes;
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        R.krw[r] = __ldg(reinterpret_cast<const uint4*>(regb + ((slot >> 4) * 4 + 2 * half + r) * 128 + (slot & 7) * 16));
+    }
+    // one word of region D per thread: page tid/64 of the tile, channel tid%64
+    const int kpos = t0 + (tid >> 6) * p.P;
+    R.krm = 0u;
+    if ((tid >> 6) * p.P < kTcTok && kpos < hi)
+      R.krm = __ldg(reinterpret_cast<const uint32_t*>(page_base(kpos) + P * (G::kRowBytes + 48)) + (tid & 63));
+  };
+
+  load_tile(0);  // (its latency overlaps the query's conversion)
+
   // ---- query: FP16, per-head power-of-two prescale 2^E, divided by the field weight of the
   // code operand at each tile position; per-group sums for the minimum terms. The BF16 rows are
   // in the tile region: bulk-copied at the start, or copied here with one batch of independent
@@ -406,48 +450,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
       }
     }
   }
-
-  // ---- per-tile packed loads (issued one tile ahead)
-  const size_t P = static_cast<size_t>(p.P);
-  auto page_base = [&](int pos) -> const uint8_t* {
-    const int pg = pos >> p.p_shift;
-    const int32_t pid = pg - pg0 < kPidCache ? pids[pg - pg0]
-                                             : __ldg(p.page_table + static_cast<size_t>(b) * p.max_pages + pg);
-    return p.pool + static_cast<size_t>(pid) * static_cast<size_t>(p.page_bytes);
-  };
-  TileRegs<BITS> R;
-  auto load_tile = [&](int i) {
-    const int t0 = (tile_begin + i) * kTcTok;
-#pragma unroll
-    for (int it = 0; it < G::kItems; ++it) {
-      const int tb = G::tb_of(warp, it), jb = G::jb_of(it);
-      const int t = 8 * tb + (lane & 7), j = 4 * jb + (lane >> 3);
-      const int pos = t0 + t;
-      R.lat[it] = make_uint4(0u, 0u, 0u, 0u);
-      if (pos < hi) {
-        const uint8_t* base = page_base(pos);
-        const int slot = pos & (p.P - 1);
-        R.lat[it] = __ldg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(slot) * G::kRowBytes +
-                                                         16 * (j ^ (slot & 7))));
-      }
-    }
-    const int pos = t0 + 32 * quarter + lane;
-    R.tmeta = R.krw[0] = R.krw[1] = make_uint4(0u, 0u, 0u, 0u);
-    if (pos < hi) {
-      const uint8_t* base = page_base(pos);
-      const int slot = pos & (p.P - 1);
-      R.tmeta = __ldg(reinterpret_cast<const uint4*>(base + P * (G::kRowBytes + 32) + slot * 16));
-      const uint8_t* regb = base + P * G::kRowBytes;
-#pragma unroll
-      for (int r = 0; r < 2; ++r)
-        R.krw[r] = __ldg(reinterpret_cast<const uint4*>(regb + ((slot >> 4) * 4 + 2 * half + r) * 128 + (slot & 7) * 16));
-    }
-    // one word of region D per thread: page tid/64 of the tile, channel tid%64
-    const int kpos = t0 + (tid >> 6) * p.P;
-    R.krm = 0u;
-    if ((tid >> 6) * p.P < kTcTok && kpos < hi)
-      R.krm = __ldg(reinterpret_cast<const uint32_t*>(page_base(kpos) + P * (G::kRowBytes + 48)) + (tid & 63));
-  };
 
   uint32_t tmem = 0;
   // codes of the latent into the tile as weighted FP16 subnormals; k_R values into tensor
@@ -555,7 +557,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
       }
   };
 
-  load_tile(0);
   krm_s[tid] = R.krm;
   if (half == 0) tm_s[32 * quarter + lane] = R.tmeta;
   tc_fence_before();
