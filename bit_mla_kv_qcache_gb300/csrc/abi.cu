@@ -50,7 +50,7 @@ size_t mla_qcache_workspace_bytes(const mla_qcache_config* cfg, int32_t B, int32
   if (check_config(cfg) != MLA_QCACHE_OK || B < 1 || H < 16 || H > 256 || H % 16 || max_pages < 1) return 0;
   int sms = 0;
   if (current_sm_count(&sms) != MLA_QCACHE_OK) return 0;
-  const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, sms);
+  const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, cfg->n_sink, cfg->n_recent, sms);
   const int nq = mlaq::decode_num_protected(B, H, max_pages, cfg->page_size, cfg->n_sink, cfg->n_recent, sms);
   return mlaq::decode_workspace_bytes(B, H, ns + nq);
 }
@@ -208,7 +208,7 @@ int mla_qcache_decode_plan(const mla_qcache_config* cfg, int32_t B, int32_t H, i
   if (st != MLA_QCACHE_OK) return st;
   if (!plan) return MLA_QCACHE_ERR_NULL;
   if (B < 1 || H < 16 || H > 256 || H % 16 || max_pages < 1 || num_sms < 1) return MLA_QCACHE_ERR_SHAPE;
-  const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, num_sms);
+  const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, cfg->n_sink, cfg->n_recent, num_sms);
   const int nq = mlaq::decode_num_protected(B, H, max_pages, cfg->page_size, cfg->n_sink, cfg->n_recent, num_sms);
   plan[0] = ns;
   plan[1] = nq;
@@ -225,7 +225,7 @@ int mla_qcache_decode_launches(const mla_qcache_config* cfg, int32_t B, int32_t 
   int sms = 0;
   const int st2 = current_sm_count(&sms);
   if (st2 != MLA_QCACHE_OK) return st2;
-  const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, sms);
+  const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, cfg->n_sink, cfg->n_recent, sms);
   const int nq = mlaq::decode_num_protected(B, H, max_pages, cfg->page_size, cfg->n_sink, cfg->n_recent, sms);
   const int slots = mlaq::decode_share_slots(B, H, max_pages, cfg->page_size, ns, nq, sms);
   const int n = mlaq::decode_launch_count(cfg->bits_c, B, H, ns, nq, slots);
@@ -307,7 +307,7 @@ static int decode_impl(const mla_qcache_config* cfg, int32_t B, int32_t H, int32
   int sms = 0;
   st = current_sm_count(&sms);
   if (st != MLA_QCACHE_OK) return st;
-  const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, sms);
+  const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, cfg->n_sink, cfg->n_recent, sms);
   const int nq = mlaq::decode_num_protected(B, H, max_pages, cfg->page_size, cfg->n_sink, cfg->n_recent, sms);
   const size_t need = mlaq::decode_workspace_bytes(B, H, ns + nq);
   if (workspace_bytes < need) return MLA_QCACHE_ERR_WORKSPACE;
@@ -462,7 +462,7 @@ int mla_qcache_decode_attn_noalloc(const mla_qcache_config* cfg, int32_t B, int3
   int sms = 0;
   st = current_sm_count(&sms);
   if (st != MLA_QCACHE_OK) return st;
-  const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, sms);
+  const int ns = mlaq::decode_num_splits(B, H, max_pages, cfg->page_size, cfg->n_sink, cfg->n_recent, sms);
   const int nq = mlaq::decode_num_protected(B, H, max_pages, cfg->page_size, cfg->n_sink, cfg->n_recent, sms);
   if (mlaq::decode_workspace_bytes(B, H, ns + nq) > mlaq::kNoAllocScratchBytes) return MLA_QCACHE_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;

@@ -1461,11 +1461,12 @@ cudaError_t launch_combine(const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-int decode_num_splits(int B, int H, int max_pages, int P, int num_sms) {
+int decode_num_splits(int B, int H, int max_pages, int P, int S, int W, int num_sms) {
   if (decode_uses_tc(H)) return decode_tc_num_splits(B, H, max_pages, P, num_sms);
   const int groups = B * (H / 16);
   const int target = kCtasPerSm * num_sms;  // one full wave of resident CTAs
-  int ns = target / (groups > 0 ? groups : 1) - 1;
+  // one wave holds the packed shares and the protected CTAs of every sequence-head block
+  int ns = target / (groups > 0 ? groups : 1) - decode_num_protected(B, H, max_pages, P, S, W, num_sms);
   const long long max_sub = (static_cast<long long>(max_pages) * P) / kPT;
   // Long page tables get splits of at most ~kShareTiles tiles even past one wave: a ragged batch
   // then spreads its longest sequences over many CTAs while the shares of short sequences are

@@ -145,7 +145,7 @@ __device__ __forceinline__ int decode_seq_len(const DecodeParams& p, int b, int&
 
 // Number of packed-token shares, and of CTAs for the protected tokens, of each (sequence,
 // 16-head block) for a problem size (depends on the SM count).
-int decode_num_splits(int B, int H, int max_pages, int P, int num_sms);
+int decode_num_splits(int B, int H, int max_pages, int P, int S, int W, int num_sms);
 int decode_num_protected(int B, int H, int max_pages, int P, int S, int W, int num_sms);
 // Workspace layout of a decode call: kArriveBytes of merge counters (zero between calls), then the
 // partial outputs and the partial maxima and sums.

@@ -188,10 +188,18 @@ def test_decode_plan_shapes(L):
     p = L.decode_plan(c4, 32, 16, 66, sms)
     assert (p["n_split"], p["n_protected"], p["share_slots"], p["tensor_memory"]) == (13, 1, 0, False)
     assert 32 * (p["n_split"] + p["n_protected"]) <= wave
-    # one sequence at 16 heads over a long table takes a whole wave of shares (not 64)
-    for mp in (514, 2050, 8194):
+    # one sequence at 16 heads over a long table takes a whole wave of shares (not 64), the
+    # protected CTAs included (several of them when the packed work per share is small)
+    for mp in (513, 514, 2050, 8194):
         p = L.decode_plan(c4, 1, 16, mp, sms)
-        assert p["n_split"] == wave - 1 and p["share_slots"] == 0
+        assert p["n_split"] == wave - p["n_protected"] and p["share_slots"] == 0
+    assert L.decode_plan(c4, 1, 16, 513, sms)["n_protected"] > 1
+    # a one-wave plan never launches more CTAs than one wave holds
+    for B in (1, 2, 3, 4, 8, 16, 32):
+        for mp in (2, 9, 33, 129, 236, 257, 385, 513, 1025):
+            p = L.decode_plan(c4, B, 16, mp, sms)
+            if p["share_slots"] == 0:
+                assert B * (p["n_split"] + p["n_protected"]) <= wave, (B, mp, p)
     # the minimum share: four 32-token tiles, except for one or two sequence-head groups: one
     # tile for short tables (up to 96 tiles), two up to 384, four beyond
     p = L.decode_plan(c4, 8, 16, 10, sms)
