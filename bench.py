@@ -615,10 +615,10 @@ def e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream):
     """The step end to end through the public API: every step copies its new tokens and queries
     from pinned host memory to the device (one copy: staged contiguously, as a serving loop
     would), runs the fused write and the decode on the same rotated layer caches as the timed
-    steps, and copies O and LSE back to pinned host memory (one copy). The copies run on one copy
-    stream, double-buffered, so that step k+2's inputs arrive and step k's results leave while
-    step k+1 computes (the dependencies are explicit events, one per step into the compute); the
-    whole timed sequence of steps is captured once as a CUDA graph and replayed."""
+    steps, and copies O and LSE back to pinned host memory (one copy). The copies are
+    double-buffered on the writer's forked stream: while step k decodes, step k-1's results leave
+    and step k+1's inputs arrive, and the step's own join orders them; the whole timed sequence
+    of steps is captured once as a CUDA graph and replayed."""
     import torch
     B, H = w.batch, w.heads
     NL = len(caches)
@@ -641,25 +641,24 @@ def e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream):
                       dr[:n_out].view(B, H, 512), dr[n_out:].view(B, H)))
     cu1 = torch.arange(B + 1, dtype=torch.int32, device=dev)
     ws_buf = caches[0].workspace(H)
-    s_cp, s_wr = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    s_wr = torch.cuda.Stream(device=dev)
     # steps per graph: whole rounds over the layers, each layer an even number of times, so the
     # two length arrays of every layer are back in their starting roles after each replay
     K = 2 * NL * max(1, math.ceil(max(10, args.steps // 2) / (2 * NL)))
     k0 = sum(uses)
-    n_ev = K + 2
-    ev_ready = [torch.cuda.Event() for _ in range(n_ev)]
-    ev_comp = [torch.cuda.Event() for _ in range(n_ev)]
 
-    # One copy stream carries both directions, so that a step's compute waits on one event: step
-    # k+2's inputs are copied into slot k&1 right after step k's results have been read back
-    # from it (both once step k is done); that event then also says that the output slot is free.
+    # The copies ride on the writer's stream, inside the fork and join every step already has:
+    # during step k that stream reads back step k-1's results, copies step k+1's inputs into the
+    # slot step k-1 used, then runs step k's write, all beside step k's decode; the join at the
+    # end of step k therefore also says that step k+1's inputs arrived. No event beyond the step's
+    # own fork and join is waited on.
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        s_cp.wait_stream(stream)
-        with torch.cuda.stream(s_cp):
+        s_wr.wait_stream(stream)
+        with torch.cuda.stream(s_wr):
             for k in range(min(2, K)):
                 d_in[k].copy_(h_in, non_blocking=True)
-                ev_ready[k].record(s_cp)
+        stream.wait_stream(s_wr)
         for k in range(K):
             slot = k & 1
             layer = (k0 + k) % NL
@@ -667,24 +666,23 @@ def e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream):
             lens_in, lens_out = (cache.seq_lens, alt) if uses[layer] % 2 == 0 else (alt, cache.seq_lens)
             uses[layer] += 1
             d_c, d_k, d_ql, d_qr, out, lse = views[slot]
-            stream.wait_event(ev_ready[k])  # this step's inputs arrived, its output slot is free
             ev_fork = torch.cuda.Event()
-            ev_fork.record(stream)  # the write forks off once the step's inputs arrived
+            ev_fork.record(stream)  # the write forks off at the step's start
             q.mla_qcache_decode_attn_pending(cfg, d_ql, d_qr, cache.page_table, lens_in, d_c, d_k, cu1, 1, cache.pool,
                                              cache.sink, cache.ring, w.softmax_scale, out, lse, ws_buf, cache.err,
                                              stream)
             s_wr.wait_event(ev_fork)
+            with torch.cuda.stream(s_wr):
+                if k >= 1:
+                    h_res[slot ^ 1].copy_(d_res[slot ^ 1], non_blocking=True)  # step k-1's O and LSE
+                    if k + 1 < K:
+                        d_in[slot ^ 1].copy_(h_in, non_blocking=True)  # step k+1's inputs
             q.mla_qcache_write_advance(cfg, d_c, d_k, cu1, lens_in, lens_out, 1, cache.page_table, cache.pool,
                                        cache.sink, cache.ring, cache.err, s_wr)
-            stream.wait_stream(s_wr)  # joined: the next step reads what this write stored
-            ev_comp[k].record(stream)
-            with torch.cuda.stream(s_cp):
-                s_cp.wait_event(ev_comp[k])
-                h_res[slot].copy_(d_res[slot], non_blocking=True)
-                if k + 2 < K:
-                    d_in[slot].copy_(h_in, non_blocking=True)
-                    ev_ready[k + 2].record(s_cp)
-        stream.wait_stream(s_cp)
+            stream.wait_stream(s_wr)  # joined: the next step reads what this write stored, and its inputs
+        with torch.cuda.stream(s_wr):
+            s_wr.wait_stream(stream)
+            h_res[(K - 1) & 1].copy_(d_res[(K - 1) & 1], non_blocking=True)  # the last step's results
         stream.wait_stream(s_wr)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -701,9 +699,9 @@ def e2e_measure(args, w, q, caches, lens_alt, uses, cfg, inp, dev, stream):
     return {"value": us, "unit": "us/layer", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
             "note": "public C ABI calls (fused write with the length update on a forked stream, concurrent with "
                     "the decode of the pending rows) with one H2D copy of the step's inputs and one D2H copy of O "
-                    "and LSE per step, both on one copy stream double-buffered against the compute (a step waits "
-                    "on one event: its inputs arrived and its output slot was read back), layer caches rotated "
-                    "as in the timed steps; the timed steps form one CUDA graph"}
+                    "and LSE per step, double-buffered on the forked stream (during step k: step k-1's results "
+                    "back, step k+1's inputs in, then step k's write; the step's join orders them), layer caches "
+                    "rotated as in the timed steps; the timed steps form one CUDA graph"}
 
 
 # ------------------------------------------------------------------ latency sweep against BF16
