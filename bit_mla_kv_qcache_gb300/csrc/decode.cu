@@ -1476,10 +1476,10 @@ int decode_num_splits(int B, int H, int max_pages, int P, int S, int W, int num_
   // (the rule only ever raises the count: a wave of shorter shares stays as it is)
   if (by_len > ns && ns < 64) ns = static_cast<int>(by_len > 64 ? 64 : by_len);
   // Minimum tiles per share: at least four (each share's partial costs the merge 2 KB per head),
-  // except for up to eight sequence-head groups, whose latency is their longest share: there
-  // short tables take one-tile shares and medium ones two (their partials are then many, and
-  // merged inside the decode launch).
-  const long long min_tiles = groups > 8 ? 4 : (max_sub <= 96 ? 1 : (max_sub <= 384 ? 2 : 4));
+  // except for up to 32 sequence-head groups, whose latency is their longest share: there short
+  // tables take one-tile shares and medium ones two (their partials are then many, merged inside
+  // the decode launch where they are 24 or more).
+  const long long min_tiles = groups > 32 ? 4 : (max_sub <= 96 ? 1 : (max_sub <= 384 ? 2 : 4));
   int cap = static_cast<int>(max_sub / min_tiles);
   if (cap < 1) cap = 1;
   if (ns > cap) ns = cap;

@@ -200,10 +200,10 @@ def test_decode_plan_shapes(L):
             p = L.decode_plan(c4, B, 16, mp, sms)
             if p["share_slots"] == 0:
                 assert B * (p["n_split"] + p["n_protected"]) <= wave, (B, mp, p)
-    # the minimum share: four 32-token tiles, except for up to eight sequence-head groups: one
+    # the minimum share: four 32-token tiles, except for up to 32 sequence-head groups: one
     # tile for short tables (up to 96 tiles), two up to 384, four beyond
-    p = L.decode_plan(c4, 16, 16, 10, sms)
-    assert p["n_split"] == 10 * 128 // 32 // 4
+    p = L.decode_plan(c4, 33, 16, 6, sms)
+    assert p["n_split"] == 6 * 128 // 32 // 4
     p = L.decode_plan(c4, 8, 16, 10, sms)
     assert p["n_split"] == 10 * 128 // 32
     p = L.decode_plan(c4, 4, 16, 30, sms)

@@ -74,7 +74,7 @@ CASES = [
     (C4, [1], 16, 2),
     (C2, [2100, 64, 777], 32, 1),
     (C4, [1200, 1201], 48, 1),
-    (C4, [300, 250, 384, 100, 200, 300, 333, 17, 300, 290, 64, 380], 16, 2),
+    (C4, [300, 250, 384, 100, 200, 300, 333, 17, 300, 290, 64, 380], 48, 2),
     (C4, [900, 300], 128, 3),
 ]
 
