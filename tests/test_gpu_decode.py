@@ -134,6 +134,32 @@ def test_query_alignment_does_not_change_the_result(w, heads):
     gu.check_decode(out_u, lse_u, o_ref, l_ref, TOL)
 
 
+@pytest.mark.parametrize("heads", [16, 64])
+def test_unused_page_table_entries_are_never_checked(heads):
+    """Entries of the page table past a sequence's pages may hold anything (the 16-head kernel
+    copies short tables whole, before the length is known): no error bit, the same result."""
+    lens = [700, 300, 0]
+    inp = workloads.make_inputs(C4, seq_lens=np.array(lens, np.int32), extra_pages=3, heads=heads)
+    kw = C4.config_kwargs()
+    cache = gu.gpu_cache(kw, inp)
+    gu.write_rows(cache, inp.c, inp.kr, inp.seq_lens, max(lens))
+    pt = inp.page_table.copy()
+    for b, T in enumerate(lens):
+        used = -(-T // C4.page_size)
+        pt[b, used:] = np.where(np.arange(pt.shape[1] - used) % 2 == 0, -7, 10 ** 6)
+    cache.page_table.copy_(torch.from_numpy(pt))
+    out, lse = cache.decode(gu.dev(inp.q_lat), gu.dev(inp.q_rope), C4.softmax_scale)
+    torch.cuda.synchronize()
+    assert cache.error_bits() == 0, cache.error_bits()
+    cfg, pool, sink, ring = gu.oracle_cache(kw, inp)
+    assert oracle.write(cfg, inp.c, inp.kr, inp.cu, np.zeros(len(lens), np.int32), max(lens), inp.page_table,
+                        pool, sink, ring) == 0
+    o_ref, l_ref, fl = oracle.decode(cfg, inp.q_lat, inp.q_rope, pt, inp.seq_lens, pool, sink, ring,
+                                     C4.softmax_scale)
+    assert fl == 0
+    gu.check_decode(out, lse, o_ref, l_ref, TOL)
+
+
 def test_bad_page_sets_error_bit():
     inp = workloads.make_inputs(C4, seq_lens=np.array([700], np.int32))
     kw = C4.config_kwargs()
