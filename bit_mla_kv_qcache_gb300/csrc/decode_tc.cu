@@ -3,26 +3,30 @@
 // appendix Table 5).
 //
 // Grid (B, H/64, n_split). CTA (b, hq, split) handles heads 64hq .. 64hq+63 of sequence b over
-// share `split` of the packed tokens [S, T-W), in tiles of 128 tokens. Per tile:
-//   1. scores, exact products: the latent codes enter a shared-memory tile as FP16 subnormals
-//      (a masked code field n at bit offset k of a half is exactly n * 2^(k-24)); the query
-//      carries the inverse field weight, so per latent group g the tensor cores produce
-//      R_g[t][h] = 2^(E-24) sum_{c in g} q_c code_tc  (tcgen05.mma kind::f16, FP32 in tensor
-//      memory). The threads, one token per lane, apply the token's group scale and minimum in
-//      FP32: score = sum_g (scale_tg R_g + min_tg 2^(E-24) sum_{c in g} q_c) + k_R part. k_R is
-//      dequantized (per-channel page scale and minimum) into tensor memory as a high and a low
-//      FP16 part, so its products carry ~2^-22 relative error;
-//   2. softmax on the scores (one token per lane), running max per head raised only when a
+// share `split` of the packed tokens [S, T-W), in tiles of 128 tokens; thread (lane t, half h)
+// loads token t's code chunks of channel half h of every latent group. Per tile:
+//   1. scores, exact products, one latent group at a time: the group's codes enter tensor memory
+//      as FP16 subnormals (a masked code field n at bit offset k of a half is exactly
+//      n * 2^(k-24)), the A operand of tcgen05.mma kind::f16; the query (B, in shared memory)
+//      carries the inverse field weight, so the tensor cores produce
+//      R_g[t][h] = 2^(E-24) sum_{c in g} q_c code_tc (FP32 in tensor memory, two accumulators so
+//      one group drains while the next is multiplied). The threads, one token per lane, apply
+//      the token's group scale and minimum in FP32:
+//      score = sum_g (scale_tg R_g + min_tg 2^(E-24) sum_{c in g} q_c) + k_R part. k_R is
+//      dequantized (per-channel page scale and minimum) into the same tensor-memory operand as
+//      a high and a low FP16 part, so its products carry ~2^-22 relative error. The score
+//      products read only the query from shared memory, whose port the readout's operands need;
+//   2. while the groups are scored, their dequantized values v = scale * code + min (FP16, one
+//      rounding) go to a shared-memory tile, token-major;
+//   3. softmax on the scores (one token per lane), running max per head raised only when a
 //      score exceeds it by more than 2^8 (weights stay <= 2^8 in FP16);
-//   3. readout O^T[512 ch x 64 heads] += V^T . P: once the score products are done the same
-//      tile is rewritten with the dequantized values v = scale * code + min (FP16, one rounding)
-//      and read channel-major; B = the weights stored heads-contiguous. O accumulates in tensor
-//      memory over the share.
-// Operands use the no-swizzle canonical layout of 8x8 core matrices (128 B each): one token's
-// 8 channels per 16-byte row, so one tile is the K-major operand of the scores and the M-major
-// operand of the readout. The latent channels inside each 8 (INT4) or 16 (INT2) channel block
-// are in the order the unpack produces them; the query follows that order and the epilogue
-// writes each output row to its own channel.
+//   4. readout O^T[512 ch x 64 heads] += V^T . P: the value tile read channel-major (M-major A),
+//      B = the weights stored heads-contiguous. O accumulates in tensor memory over the share.
+// Shared-memory operands use the no-swizzle canonical layout of 8x8 core matrices (128 B each):
+// one token's 8 channels per 16-byte row. The latent channels inside each 8 (INT4) or 16 (INT2)
+// channel block are in the order the unpack produces them (the same order in the tensor-memory
+// codes and the value tile); the query follows that order and the epilogue writes each output
+// row to its own channel.
 // The protected (BF16) tokens are handled by the 16-head kernel's protected CTAs; the merge
 // kernel combines every partial.
 #include <cuda_fp16.h>
@@ -52,10 +56,9 @@ constexpr int kTmemSlotOff = kMiscOff + 32;
 constexpr int kMOff = kMiscOff + 64;              // running max per head (log2 units)
 constexpr int kHsOff = kMOff + 256;               // MMA score -> log2 units, per head
 constexpr int kRedOff = kHsOff + 256;             // [4 lane quarters][64 heads] floats
-constexpr int kQsOff = kRedOff + 1024;            // [64 heads][4 groups] 2^(E-24) sum_{c in g} q_c
+constexpr int kQsOff = kRedOff + 1024;            // [4 groups][64 heads] 2^(E-24) sum_{c in g} q_c
 constexpr int kKrmOff = kQsOff + 1024;           // k_R (scale, min) of the tile's pages [4][64]
-constexpr int kTmOff = kKrmOff + 1024;           // latent (scale, min) of the tile's tokens [128][4]
-constexpr int kPidOff = kTmOff + 2048;           // page ids of the share (first kPidCache)
+constexpr int kPidOff = kKrmOff + 1024;          // page ids of the share (first kPidCache)
 constexpr int kPidCache = 256;
 constexpr int kTcSmem = kPidOff + 4 * kPidCache;
 static_assert(kTcSmem <= 227 * 1024, "one CTA per SM");
@@ -72,8 +75,10 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;       // O^T of latent group g (128 channels x 64 heads) at 64 g
 constexpr uint32_t kColSA = 256;    // score buffers S^T (128 tokens x 64 heads)
 constexpr uint32_t kColSB = 320;
-constexpr uint32_t kColKrHi = 384;  // k_R operand, high FP16 parts: 128 tokens x 64 channels, a pair per column
-constexpr uint32_t kColKrLo = 416;  // k_R operand, low FP16 parts
+constexpr uint32_t kColA = 384;     // A operand of the score products: one latent group's codes (128 tokens
+                                    // x 128 channels, a pair per column), then k_R:
+constexpr uint32_t kColKrHi = 384;  // k_R high FP16 parts: 128 tokens x 64 channels, a pair per column
+constexpr uint32_t kColKrLo = 416;  // k_R low FP16 parts
 constexpr uint32_t kColL = 448;     // per-token-lane partial sums of the weights, 64 heads
 
 // instruction descriptors (kind::f16): D FP32, A/B FP16, M = 128, N = 64
@@ -188,9 +193,9 @@ __device__ __forceinline__ float lds_f32(const float* p) {
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_addr(p)));
   return v;
 }
-__device__ __forceinline__ float2 lds_f32x2(const float* p) {
-  float2 v;
-  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(smem_addr(p)));
+__device__ __forceinline__ float4 lds_f32x4(const float* p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(smem_addr(p)));
   return v;
 }
 
@@ -203,19 +208,17 @@ struct TcGeom {
   static constexpr int kRowBytes = 64 * BITS;                   // region A bytes per token
   static constexpr int kChunks = kRowBytes / 16;                // 16-byte chunks per token
   static constexpr int kItems = kTcTok * kChunks / kTcThreads;  // latent chunks per thread and tile
-  static constexpr int kJb = kChunks / 4;                       // chunk quads per token (4 or 2)
-  // item `it` of warp w: token block tb (8 tokens), chunk quad jb (lanes take chunk 4 jb + lane/8);
-  // each warp's items cover every quad, so each half of the groups is half of every warp's work
-  __device__ static int jb_of(int it) { return it % kJb; }
-  __device__ static int tb_of(int warp, int it) { return (warp * kItems + it) / kJb; }
-  // whether item `it` lies in latent groups 0 and 1 (INT4: quads 0-1; INT2: quad 0)
-  __host__ __device__ static constexpr bool low_groups(int it) { return (it % kJb) < kJb / 2; }
+  static constexpr int kCpg = kItems / 4;                       // chunks per latent group and channel half
+  // Thread (token lane t, channel half h) holds, for each latent group g, the kCpg chunks of
+  // channels 128 g + 64 h .. 128 g + 64 h + 63 of token t; item it = kCpg g + c.
+  __device__ static int chunk_of(int half, int it) { return (it / kCpg) * (kChunks / 4) + half * kCpg + it % kCpg; }
 };
+static_assert(TcGeom<4>::kCpg * 32 * 4 == 256 && TcGeom<2>::kCpg * 64 * 4 == 256, "a channel half of a group per thread");
 
 // The packed data one thread unpacks for one tile, loaded a tile ahead.
 template <int BITS>
 struct TileRegs {
-  uint4 lat[TcGeom<BITS>::kItems];     // latent code chunks (unpacked twice: codes, then values)
+  uint4 lat[TcGeom<BITS>::kItems];     // latent code chunks of this lane's token (unpacked twice)
   uint4 tmeta;                         // (scale, min) of the 4 groups of this lane's token
   uint4 krw[2];                        // k_R code words of this lane's token, 32 channels
   uint32_t krm;                        // one k_R (scale, min) word of the tile's pages (staged)
@@ -236,7 +239,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
   float* qs = reinterpret_cast<float*>(smem + kQsOff);
   int32_t* pids = reinterpret_cast<int32_t*>(smem + kPidOff);
   uint32_t* krm_s = reinterpret_cast<uint32_t*>(smem + kKrmOff);
-  uint4* tm_s = reinterpret_cast<uint4*>(smem + kTmOff);
   const uint32_t tile_a = smem_addr(smem + kTileOff), q_a = smem_addr(smem + kQOff), p_a = smem_addr(smem + kPOff);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -329,24 +331,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
   TileRegs<BITS> R;
   auto load_tile = [&](int i) {
     const int t0 = (tile_begin + i) * kTcTok;
-#pragma unroll
-    for (int it = 0; it < G::kItems; ++it) {
-      const int tb = G::tb_of(warp, it), jb = G::jb_of(it);
-      const int t = 8 * tb + (lane & 7), j = 4 * jb + (lane >> 3);
-      const int pos = t0 + t;
-      R.lat[it] = make_uint4(0u, 0u, 0u, 0u);
-      if (pos < hi) {
-        const uint8_t* base = page_base(pos);
-        const int slot = pos & (p.P - 1);
-        R.lat[it] = __ldg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(slot) * G::kRowBytes +
-                                                         16 * (j ^ (slot & 7))));
-      }
-    }
     const int pos = t0 + 32 * quarter + lane;
     R.tmeta = R.krw[0] = R.krw[1] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int it = 0; it < G::kItems; ++it) R.lat[it] = make_uint4(0u, 0u, 0u, 0u);
     if (pos < hi) {
       const uint8_t* base = page_base(pos);
       const int slot = pos & (p.P - 1);
+      const uint8_t* row = base + static_cast<size_t>(slot) * G::kRowBytes;
+#pragma unroll
+      for (int it = 0; it < G::kItems; ++it)
+        R.lat[it] = __ldg(reinterpret_cast<const uint4*>(row + 16 * (G::chunk_of(half, it) ^ (slot & 7))));
       R.tmeta = __ldg(reinterpret_cast<const uint4*>(base + P * (G::kRowBytes + 32) + slot * 16));
       const uint8_t* regb = base + P * G::kRowBytes;
 #pragma unroll
@@ -385,29 +380,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
     }
     __syncthreads();
     const int h = tid >> 2, part = tid & 3;  // 4 threads per head
-    const uint32_t* row = qlat_s + h * kQRowWords;
+    // one pass over latent group `part` (its maximum magnitude and its sum) in 16-byte reads,
+    // staggered so that the 8 threads of a quarter-warp (2 heads x 4 groups) hit distinct banks,
+    // then this thread's quarter of the k_R row
+    const uint32_t* row = qlat_s + h * kQRowWords + 64 * part;
     float mx = 0.f, gs = 0.f;
-#pragma unroll 8
-    for (int k = part; k < kLatent / 2; k += 4) {
-      const uint32_t w = row[k];
-      mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w))));
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint4 v = *reinterpret_cast<const uint4*>(row + 4 * ((k + 2 * part) & 15));
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = bf16_lo(w4[e]), hi = bf16_hi(w4[e]);
+        mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
+        gs += lo + hi;
+      }
     }
 #pragma unroll
-    for (int k = part; k < kRope / 2; k += 4) {
-      const uint32_t w = qrope_s[h * (kRope / 2) + k];
-      mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(w)), fabsf(bf16_hi(w))));
-    }
-#pragma unroll 8
-    for (int k = 64 * part; k < 64 * part + 64; ++k) {  // latent group `part`
-      const uint32_t w = row[k];
-      gs += bf16_lo(w) + bf16_hi(w);
+    for (int k = 0; k < 2; ++k) {
+      const uint4 v = *reinterpret_cast<const uint4*>(qrope_s + h * (kRope / 2) + 8 * part + 4 * k);
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(w4[e])), fabsf(bf16_hi(w4[e]))));
     }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     bool range = false;
     const int E = prescale_exponent(mx, range);
     if (range) flags |= kErrRange;
-    qs[h * 4 + part] = gs * pow2_int(E - 24);
+    qs[part * kTcHeads + h] = gs * pow2_int(E - 24);
     if (part == 0) {
       hsc[h] = p.scale_log2 * pow2_int(24 - E);
       red[h] = static_cast<float>(E);
@@ -452,88 +453,100 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
   }
 
   uint32_t tmem = 0;
-  // codes of the latent into the tile as weighted FP16 subnormals; k_R values into tensor
-  // memory as high and low FP16 parts
-  auto unpack_codes = [&](int i) {
+  // The latent codes of group g into tensor memory as weighted FP16 subnormals: the A operand of
+  // the group's score products (lane = token, a channel pair per column, columns 4 m + r for the
+  // m-th 8-channel block of this thread's channel half).
+  auto codes_to_tmem = [&](int g) {
+    uint32_t c[2][16];
 #pragma unroll
-    for (int it = 0; it < G::kItems; ++it) {
-      const int tb = G::tb_of(warp, it), jb = G::jb_of(it);
-      const int t = 8 * tb + (lane & 7), j = 4 * jb + (lane >> 3);
-      const uint32_t w[4] = {R.lat[it].x, R.lat[it].y, R.lat[it].z, R.lat[it].w};
-      const uint32_t row = tile_a + tb * 128 + (t & 7) * 16;
+    for (int cc = 0; cc < G::kCpg; ++cc) {
+      const uint4 v = R.lat[g * G::kCpg + cc];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint32_t w8 = w[k] >> 8;
         if (BITS == 4) {
-          st_shared_v4(row + (4 * j + k) * 2048, w[k] & 0x000F000Fu, w[k] & 0x00F000F0u, w8 & 0x000F000Fu,
-                       w8 & 0x00F000F0u);
+          const int m = 4 * cc + k;
+          uint32_t* d = &c[m >> 2][4 * (m & 3)];
+          d[0] = w[k] & 0x000F000Fu;
+          d[1] = w[k] & 0x00F000F0u;
+          d[2] = w8 & 0x000F000Fu;
+          d[3] = w8 & 0x00F000F0u;
         } else {
-          const int cb = 8 * j + 2 * k;
-          st_shared_v4(row + cb * 2048, w[k] & 0x00030003u, w[k] & 0x000C000Cu, w[k] & 0x00300030u, w[k] & 0x00C000C0u);
-          st_shared_v4(row + (cb + 1) * 2048, w8 & 0x00030003u, w8 & 0x000C000Cu, w8 & 0x00300030u, w8 & 0x00C000C0u);
+          const int m = 2 * k;
+          uint32_t* d = &c[m >> 2][4 * (m & 3)];
+          d[0] = w[k] & 0x00030003u;
+          d[1] = w[k] & 0x000C000Cu;
+          d[2] = w[k] & 0x00300030u;
+          d[3] = w[k] & 0x00C000C0u;
+          d[4] = w8 & 0x00030003u;
+          d[5] = w8 & 0x000C000Cu;
+          d[6] = w8 & 0x00300030u;
+          d[7] = w8 & 0x00C000C0u;
         }
       }
     }
-    {
-      const int tt = 32 * quarter + lane;
-      const int pos = (tile_begin + i) * kTcTok + tt;
-      const int nn = ((pos & (p.P - 1)) >> 3) & 1;
-      const uint32_t* mdp = krm_s + (tt >> p.p_shift) * 64 + 32 * half;  // staged before the tile's barrier
-      uint32_t md[32];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint4 v = *reinterpret_cast<const uint4*>(mdp + 4 * k);
-        md[4 * k] = v.x;
-        md[4 * k + 1] = v.y;
-        md[4 * k + 2] = v.z;
-        md[4 * k + 3] = v.w;
-      }
-      uint32_t khi[16], klo[16];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const uint32_t wq[4] = {R.krw[r].x, R.krw[r].y, R.krw[r].z, R.krw[r].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t x = (wq[q] >> (4 * (2 * nn + h))) & 0x000F000Fu;
-            const int lc = 16 * r + 8 * h + 2 * q;  // local channel pair (lc, lc+1)
-            const float v0 = fmaf(half_bits_lo(md[lc]), static_cast<float>(x & 0xffu), half_bits_hi(md[lc]));
-            const float v1 = fmaf(half_bits_lo(md[lc + 1]), static_cast<float>(x >> 16), half_bits_hi(md[lc + 1]));
-            const __half2 vh = __floats2half2_rn(v0, v1);
-            const __half2 vl = __floats2half2_rn(v0 - __low2float(vh), v1 - __high2float(vh));
-            khi[lc >> 1] = *reinterpret_cast<const uint32_t*>(&vh);
-            klo[lc >> 1] = *reinterpret_cast<const uint32_t*>(&vl);
-          }
-      }
-      tmem_st16(tmem + lane_base + kColKrHi + 16 * half, khi);
-      tmem_st16(tmem + lane_base + kColKrLo + 16 * half, klo);
-    }
+    tmem_st16(tmem + lane_base + kColA + 32 * half, c[0]);
+    tmem_st16(tmem + lane_base + kColA + 32 * half + 16, c[1]);
   };
-  // dequantized latent values v = scale * code + min into the tile (the readout operand)
-  auto unpack_values = [&](bool low) {
-    constexpr uint32_t kMagic = 0x64006400u;
+  // k_R of tile i into tensor memory (the same columns, once the latent score products are done)
+  // as high and low FP16 parts
+  auto unpack_kr = [&](int i) {
+    const int tt = 32 * quarter + lane;
+    const int pos = (tile_begin + i) * kTcTok + tt;
+    const int nn = ((pos & (p.P - 1)) >> 3) & 1;
+    const uint32_t* mdp = krm_s + (tt >> p.p_shift) * 64 + 32 * half;  // staged before a barrier
+    uint32_t md[32];
 #pragma unroll
-    for (int it = 0; it < G::kItems; ++it) {
-      if (G::low_groups(it) != low) continue;
-      const int tb = G::tb_of(warp, it), jb = G::jb_of(it);
-      const int t = 8 * tb + (lane & 7), j = 4 * jb + (lane >> 3);
-      uint32_t w[4] = {R.lat[it].x, R.lat[it].y, R.lat[it].z, R.lat[it].w};
-      const uint4 tmv = tm_s[t];  // (scale, min) of the token's 4 groups, staged before the tile's barrier
-      const int g = j / (G::kChunks / 4);
-      uint32_t lm = g == 0 ? tmv.x : g == 1 ? tmv.y : g == 2 ? tmv.z : tmv.w;
-      // one chunk at a time: its arithmetic is not hoisted above the previous chunk's stores
-      asm volatile("" : "+r"(w[0]), "+r"(w[1]), "+r"(w[2]), "+r"(w[3]), "+r"(lm)::"memory");
-      const uint32_t s2 = prmt(lm, 0u, 0x1010u), m2 = prmt(lm, 0u, 0x3232u);
-      const uint32_t row = tile_a + tb * 128 + (t & 7) * 16;
+    for (int k = 0; k < 8; ++k) {
+      const uint4 v = *reinterpret_cast<const uint4*>(mdp + 4 * k);
+      md[4 * k] = v.x;
+      md[4 * k + 1] = v.y;
+      md[4 * k + 2] = v.z;
+      md[4 * k + 3] = v.w;
+    }
+    uint32_t khi[16], klo[16];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const uint32_t wq[4] = {R.krw[r].x, R.krw[r].y, R.krw[r].z, R.krw[r].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t x = (wq[q] >> (4 * (2 * nn + h))) & 0x000F000Fu;
+          const int lc = 16 * r + 8 * h + 2 * q;  // local channel pair (lc, lc+1)
+          const float v0 = fmaf(half_bits_lo(md[lc]), static_cast<float>(x & 0xffu), half_bits_hi(md[lc]));
+          const float v1 = fmaf(half_bits_lo(md[lc + 1]), static_cast<float>(x >> 16), half_bits_hi(md[lc + 1]));
+          const __half2 vh = __floats2half2_rn(v0, v1);
+          const __half2 vl = __floats2half2_rn(v0 - __low2float(vh), v1 - __high2float(vh));
+          khi[lc >> 1] = *reinterpret_cast<const uint32_t*>(&vh);
+          klo[lc >> 1] = *reinterpret_cast<const uint32_t*>(&vl);
+        }
+    }
+    tmem_st16(tmem + lane_base + kColKrHi + 16 * half, khi);
+    tmem_st16(tmem + lane_base + kColKrLo + 16 * half, klo);
+  };
+  // dequantized values v = scale * code + min of group g into the shared-memory tile (the
+  // readout's operand): this lane's token, this thread's channel half; a warp's 32 tokens fill
+  // 512 contiguous bytes of each 8-channel block
+  auto values_to_smem = [&](int g) {
+    constexpr uint32_t kMagic = 0x64006400u;
+    const uint32_t lm = g == 0 ? R.tmeta.x : g == 1 ? R.tmeta.y : g == 2 ? R.tmeta.z : R.tmeta.w;
+    const uint32_t s2 = prmt(lm, 0u, 0x1010u), m2 = prmt(lm, 0u, 0x3232u);
+    const uint32_t row = tile_a + 16 * (32 * quarter + lane);
+#pragma unroll
+    for (int cc = 0; cc < G::kCpg; ++cc) {
+      const uint4 v = R.lat[g * G::kCpg + cc];
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         if (BITS == 4) {
-          st_shared_v4(row + (4 * j + k) * 2048, dq2((w[k] & 0x000F000Fu) | kMagic, s2, m2),
+          const int cb = 16 * g + 8 * half + 4 * cc + k;
+          st_shared_v4(row + cb * 2048, dq2((w[k] & 0x000F000Fu) | kMagic, s2, m2),
                        dq2(((w[k] >> 4) & 0x000F000Fu) | kMagic, s2, m2), dq2(((w[k] >> 8) & 0x000F000Fu) | kMagic, s2, m2),
                        dq2(((w[k] >> 12) & 0x000F000Fu) | kMagic, s2, m2));
         } else {
-          const int cb = 8 * j + 2 * k;
+          const int cb = 16 * g + 8 * half + 2 * k;
           st_shared_v4(row + cb * 2048, dq2((w[k] & 0x00030003u) | kMagic, s2, m2),
                        dq2(((w[k] >> 2) & 0x00030003u) | kMagic, s2, m2), dq2(((w[k] >> 4) & 0x00030003u) | kMagic, s2, m2),
                        dq2(((w[k] >> 6) & 0x00030003u) | kMagic, s2, m2));
@@ -545,20 +558,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
       }
     }
   };
-  // score products of latent groups g0 (into S_A) and g0+1 (into S_B)
-  auto issue_groups = [&](int g0) {
+  // score products of latent group g (A: its codes in tensor memory; B: the query) into S_A (even
+  // g) or S_B (odd g)
+  auto issue_group = [&](int g) {
 #pragma unroll
-    for (int gg = 0; gg < 2; ++gg)
+    for (int k = 0; k < 8; ++k)
+      tc_mma_ts(tmem + ((g & 1) ? kColSB : kColSA), tmem + kColA + 8 * k, sdesc(q_a + (8 * g + k) * 2048, 1024, 128),
+                kIdescScore, k > 0);
+  };
+  // k_R products, high and low parts, into S_A
+  auto issue_kr = [&]() {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int kc = 8 * (g0 + gg) + k;
-        tc_mma_ss(tmem + (gg ? kColSB : kColSA), sdesc(tile_a + kc * 4096, 2048, 128),
-                  sdesc(q_a + kc * 2048, 1024, 128), kIdescScore, k > 0);
-      }
+    for (int kc = 0; kc < kRope / 16; ++kc) {
+      const uint64_t bq = sdesc(q_a + (kLatent / 8 + 2 * kc) * 1024, 1024, 128);
+      tc_mma_ts(tmem + kColSA, tmem + kColKrHi + 8 * kc, bq, kIdescScore, kc > 0);
+      tc_mma_ts(tmem + kColSA, tmem + kColKrLo + 8 * kc, bq, kIdescScore, true);
+    }
   };
 
   krm_s[tid] = R.krm;
-  if (half == 0) tm_s[32 * quarter + lane] = R.tmeta;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -583,11 +601,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
   int i = 0;
   for (; i < n_my; ++i) {
     const int t0 = (tile_begin + i) * kTcTok;
-    if (i > 0) {  // read by the previous tile before its readout barrier
-      krm_s[tid] = R.krm;
-      if (half == 0) tm_s[32 * quarter + lane] = R.tmeta;
+    if (i > 0) krm_s[tid] = R.krm;  // the previous tile's k_R unpack read it before its softmax barriers
+    // group 0's codes into tensor memory; its score products queue behind the previous readout
+    codes_to_tmem(0);
+    tmem_wait_st();
+    sync_issue();
+    if (tid == 0) {
+      tc_fence_after();
+      issue_group(0);
+      tc_commit(bars);
     }
-    if (o_commits > o_waits) {  // the previous readout still reads the tile and the weights
+    ++s_commits;
+    if (o_commits > o_waits) {  // the previous readout still reads the value tile and the weights
       const bool ok = mbar_wait_bounded(bars + 1, o_waits & 1, kTcWaitBudget);
       ++o_waits;
       if (__syncthreads_or(!ok)) {
@@ -596,75 +621,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
       }
       tc_fence_after();
     }
-    unpack_codes(i);
-    tmem_wait_st();
-    sync_issue();
-    if (tid == 0) {
-      tc_fence_after();
-      issue_groups(0);
-      tc_commit(bars);
-    }
-    ++s_commits;
-    // per-token group scales and minima of this lane's token
-    const uint32_t tm[4] = {R.tmeta.x, R.tmeta.y, R.tmeta.z, R.tmeta.w};
+    // per group: once its products are done, the next group's codes (after group 3: k_R) take
+    // the tensor-memory operand and are issued; then the group is drained in FP32 with this
+    // token's group scale and minimum, and its values go to the shared-memory tile
     float acc[32];
-    if (!wait_s()) {
-      aborted = true;
-      break;
-    }
-    {
-      float sv[32];
-      const float s0 = half_bits_lo(tm[0]), m0 = half_bits_hi(tm[0]), s1 = half_bits_lo(tm[1]), m1 = half_bits_hi(tm[1]);
-      tmem_ld32(tmem + lane_base + kColSA + hb0, sv);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float2 qv = lds_f32x2(qs + (hb0 + j) * 4);
-        acc[j] = fmaf(s0, sv[j], fmaf(m0, qv.x, m1 * qv.y));
+    for (int g = 0; g < 4; ++g) {
+      if (!wait_s()) {
+        aborted = true;
+        break;
       }
-      tmem_ld32(tmem + lane_base + kColSB + hb0, sv);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j] = fmaf(s1, sv[j], acc[j]);
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-      issue_groups(2);
-      tc_commit(bars);
-    }
-    ++s_commits;
-    unpack_values(true);  // groups 0 and 1: their score products are done
-    if (!wait_s()) {
-      aborted = true;
-      break;
-    }
-    {
-      float sv[32];
-      const float s2 = half_bits_lo(tm[2]), m2 = half_bits_hi(tm[2]), s3 = half_bits_lo(tm[3]), m3 = half_bits_hi(tm[3]);
-      tmem_ld32(tmem + lane_base + kColSA + hb0, sv);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float2 qv = lds_f32x2(qs + (hb0 + j) * 4 + 2);
-        acc[j] += fmaf(s2, sv[j], fmaf(m2, qv.x, m3 * qv.y));
+      if (g < 3) codes_to_tmem(g + 1);
+      else unpack_kr(i);
+      tmem_wait_st();
+      sync_issue();
+      if (tid == 0) {
+        tc_fence_after();
+        if (g < 3) issue_group(g + 1);
+        else issue_kr();
+        tc_commit(bars);
       }
-      tmem_ld32(tmem + lane_base + kColSB + hb0, sv);
+      ++s_commits;
+      {
+        const uint32_t lm = g == 0 ? R.tmeta.x : g == 1 ? R.tmeta.y : g == 2 ? R.tmeta.z : R.tmeta.w;
+        const float sg = half_bits_lo(lm), mg = half_bits_hi(lm);
+        float sv[32];
+        tmem_ld32(tmem + lane_base + ((g & 1) ? kColSB : kColSA) + hb0, sv);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j] = fmaf(s3, sv[j], acc[j]);
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {  // k_R: high and low parts into S_A (reads tensor memory and the query only)
-      tc_fence_after();
+        for (int jj = 0; jj < 8; ++jj) {
+          const float4 qv = lds_f32x4(qs + g * kTcHeads + hb0 + 4 * jj);
+          const float qq[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-      for (int kc = 0; kc < kRope / 16; ++kc) {
-        const uint64_t bq = sdesc(q_a + (kLatent / 8 + 2 * kc) * 1024, 1024, 128);
-        tc_mma_ts(tmem + kColSA, tmem + kColKrHi + 8 * kc, bq, kIdescScore, kc > 0);
-        tc_mma_ts(tmem + kColSA, tmem + kColKrLo + 8 * kc, bq, kIdescScore, true);
+          for (int e = 0; e < 4; ++e) {
+            const float t = fmaf(sg, sv[4 * jj + e], mg * qq[e]);
+            acc[4 * jj + e] = g == 0 ? t : acc[4 * jj + e] + t;
+          }
+        }
       }
-      tc_commit(bars);
+      values_to_smem(g);
     }
-    ++s_commits;
-    unpack_values(false);  // groups 2 and 3: their score products are done
+    if (aborted) break;
     if (i + 1 < n_my) load_tile(i + 1);  // every register of this tile's packed data has been used
     if (!wait_s()) {
       aborted = true;
