@@ -329,19 +329,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
     return p.pool + static_cast<size_t>(pid) * static_cast<size_t>(p.page_bytes);
   };
   TileRegs<BITS> R;
-  auto load_tile = [&](int i) {
+  // this lane's token row in region A of tile i (null past the end) and its XOR swizzle
+  auto token_row = [&](int i, int& swz) -> const uint8_t* {
+    const int pos = (tile_begin + i) * kTcTok + 32 * quarter + lane;
+    const int slot = pos & (p.P - 1);
+    swz = slot & 7;
+    return pos < hi ? page_base(pos) + static_cast<size_t>(slot) * G::kRowBytes : nullptr;
+  };
+  // the code chunks of latent group g from a token row (zero past the end)
+  auto load_group = [&](const uint8_t* row, int swz, int g) {
+#pragma unroll
+    for (int cc = 0; cc < G::kCpg; ++cc)
+      R.lat[g * G::kCpg + cc] =
+          row != nullptr ? __ldg(reinterpret_cast<const uint4*>(row + 16 * (G::chunk_of(half, g * G::kCpg + cc) ^ swz)))
+                         : make_uint4(0u, 0u, 0u, 0u);
+  };
+  // the token and page metadata of tile i and its k_R codes
+  auto load_meta = [&](int i) {
     const int t0 = (tile_begin + i) * kTcTok;
     const int pos = t0 + 32 * quarter + lane;
     R.tmeta = R.krw[0] = R.krw[1] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int it = 0; it < G::kItems; ++it) R.lat[it] = make_uint4(0u, 0u, 0u, 0u);
     if (pos < hi) {
       const uint8_t* base = page_base(pos);
       const int slot = pos & (p.P - 1);
-      const uint8_t* row = base + static_cast<size_t>(slot) * G::kRowBytes;
-#pragma unroll
-      for (int it = 0; it < G::kItems; ++it)
-        R.lat[it] = __ldg(reinterpret_cast<const uint4*>(row + 16 * (G::chunk_of(half, it) ^ (slot & 7))));
       R.tmeta = __ldg(reinterpret_cast<const uint4*>(base + P * (G::kRowBytes + 32) + slot * 16));
       const uint8_t* regb = base + P * G::kRowBytes;
 #pragma unroll
@@ -355,7 +365,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
       R.krm = __ldg(reinterpret_cast<const uint32_t*>(page_base(kpos) + P * (G::kRowBytes + 48)) + (tid & 63));
   };
 
-  load_tile(0);  // (its latency overlaps the query's conversion)
+  // the first tile, its latency overlapping the query's conversion
+  {
+    int swz;
+    const uint8_t* row = token_row(0, swz);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) load_group(row, swz, g);
+  }
+  load_meta(0);
 
   // ---- query: FP16, per-head power-of-two prescale 2^E, divided by the field weight of the
   // code operand at each tile position; per-group sums for the minimum terms. The BF16 rows are
@@ -625,6 +642,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
     // the tensor-memory operand and are issued; then the group is drained in FP32 with this
     // token's group scale and minimum, and its values go to the shared-memory tile
     float acc[32];
+    int nswz = 0;
+    const uint8_t* nrow = i + 1 < n_my ? token_row(i + 1, nswz) : nullptr;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       if (!wait_s()) {
@@ -659,9 +678,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
         }
       }
       values_to_smem(g);
+      if (i + 1 < n_my) load_group(nrow, nswz, g);  // group g's registers are free: the next tile's chunks
     }
     if (aborted) break;
-    if (i + 1 < n_my) load_tile(i + 1);  // every register of this tile's packed data has been used
+    if (i + 1 < n_my) load_meta(i + 1);  // the metadata registers are free too
     if (!wait_s()) {
       aborted = true;
       break;
