@@ -142,12 +142,18 @@ def dominant_kernel_regex(w: workloads.Workload) -> str:
     return r"decode_tc_kernel" if w.heads % 64 == 0 else r"decode_kernel"
 
 
-def source_sha() -> str:
-    """Hash of the decode kernels' sources: the DRAM traffic recorded in a decode profile holds
-    only while these are unchanged."""
+# the sources each decode kernel is compiled from: a kernel's recorded DRAM traffic holds while
+# these are unchanged
+KERNEL_SOURCES = {"decode_kernel": ("decode.cu", "kernels.cuh", "ptx.cuh"),
+                  "decode_tc_kernel": ("decode_tc.cu", "kernels.cuh", "ptx.cuh")}
+
+
+def source_sha(kernel_regex: str) -> str:
+    """Hash of the sources of the kernel that kernel_regex names."""
+    files = KERNEL_SOURCES["decode_tc_kernel" if "decode_tc" in kernel_regex else "decode_kernel"]
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_mla_kv_qcache_gb300", "csrc")
-    for f in ("decode.cu", "decode_tc.cu", "ptx.cuh"):
+    for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -166,7 +172,7 @@ def profiled_traffic(workload: str):
         return None
     with open(path) as f:
         rec = json.load(f)
-    if rec.get("source_sha") != source_sha():
+    if rec.get("source_sha") != source_sha(rec.get("kernel_regex", "")):
         return None
     return float(rec["dram_bytes_per_launch"])
 
@@ -206,7 +212,7 @@ def record_traffic(csv_path: str, workload: str, kernel_regex: str, command: str
     rec = {"workload": workload, "kernel_regex": kernel_regex, "kernels": sorted({k for _, k, _, _ in rows}),
            "launches": len(rows), "dram_bytes_read_per_launch": statistics.mean(r for _, _, r, _ in rows),
            "dram_bytes_write_per_launch": statistics.mean(w for _, _, _, w in rows),
-           "dram_bytes_per_launch": statistics.mean(per_launch), "source_sha": source_sha(), "command": command}
+           "dram_bytes_per_launch": statistics.mean(per_launch), "source_sha": source_sha(kernel_regex), "command": command}
     with open(traffic_path(workload), "w") as f:
         json.dump(rec, f, indent=1)
         f.write("\n")
