@@ -646,14 +646,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
     const uint8_t* nrow = i + 1 < n_my ? token_row(i + 1, nswz) : nullptr;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-      if (!wait_s()) {
-        aborted = true;
-        break;
-      }
+      // each thread's own wait: group g's products are done, so its code columns and the other
+      // accumulator are free; the timeout vote rides on the issue barrier (the group products
+      // read shared memory only for the query, written before the first tile's barrier)
+      const bool ok = mbar_wait_bounded(bars, s_waits & 1, kTcWaitBudget);
+      ++s_waits;
+      tc_fence_after();
       if (g < 3) codes_to_tmem(g + 1);
       else unpack_kr(i);
       tmem_wait_st();
-      sync_issue();
+      tc_fence_before();
+      if (__syncthreads_or(!ok)) {
+        aborted = true;
+        break;
+      }
       if (tid == 0) {
         tc_fence_after();
         if (g < 3) issue_group(g + 1);
