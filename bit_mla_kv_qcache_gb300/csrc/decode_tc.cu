@@ -601,10 +601,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
 
   const int hb0 = 32 * half;
   bool aborted = false;
-  int s_commits = 0, s_waits = 0, o_commits = 0, o_waits = 0;  // uniform across the CTA
+  // commits and completed waits; a wait that timed out is not counted, so that thread 0 waits for
+  // that work again (bounded) before the tensor memory is released
+  int s_commits = 0, s_waits = 0, o_commits = 0, o_waits = 0;
   auto wait_s = [&]() -> bool {
     const bool ok = mbar_wait_bounded(bars, s_waits & 1, kTcWaitBudget);
-    ++s_waits;
+    if (ok) ++s_waits;
     const bool all = !__syncthreads_or(!ok);
     tc_fence_after();
     return all;
@@ -629,13 +631,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
       tc_commit(bars);
     }
     ++s_commits;
-    if (o_commits > o_waits) {  // the previous readout still reads the value tile and the weights
-      const bool ok = mbar_wait_bounded(bars + 1, o_waits & 1, kTcWaitBudget);
-      ++o_waits;
-      if (__syncthreads_or(!ok)) {
-        aborted = true;
-        break;
-      }
+    // the previous readout still reads the value tile and the weights: each thread waits for it
+    // before its first value store (its timeout vote rides on group 0's issue barrier)
+    bool read_ok = true;
+    if (o_commits > o_waits) {
+      read_ok = mbar_wait_bounded(bars + 1, o_waits & 1, kTcWaitBudget);
+      if (read_ok) ++o_waits;
       tc_fence_after();
     }
     // per group: once its products are done, the next group's codes (after group 3: k_R) take
@@ -650,13 +651,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
       // accumulator are free; the timeout vote rides on the issue barrier (the group products
       // read shared memory only for the query, written before the first tile's barrier)
       const bool ok = mbar_wait_bounded(bars, s_waits & 1, kTcWaitBudget);
-      ++s_waits;
+      if (ok) ++s_waits;
       tc_fence_after();
       if (g < 3) codes_to_tmem(g + 1);
       else unpack_kr(i);
       tmem_wait_st();
       tc_fence_before();
-      if (__syncthreads_or(!ok)) {
+      if (__syncthreads_or(!ok || !read_ok)) {
         aborted = true;
         break;
       }
@@ -790,10 +791,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const DecodePa
     }
   } else {
     const bool ok = mbar_wait_bounded(bars + 1, o_waits & 1, kTcWaitBudget);
-    ++o_waits;
+    if (ok) ++o_waits;
     if (__syncthreads_or(!ok)) {
       flags |= kErrTimeout;
       aborted = true;
+      if (tid == 0 && o_commits > o_waits) (void)mbar_wait_bounded(bars + 1, o_waits & 1, kTcWaitBudget >> 4);
     }
   }
   tc_fence_after();
