@@ -3,6 +3,7 @@ checked against hand-counted values for the cache layout (per packed C4 token: 2
 codes, 32 B of k_R codes, 16 B of latent metadata; 256 B of k_R metadata per page; 1152 B per
 BF16 token)."""
 import math
+import os
 
 import bench
 import workloads
@@ -52,3 +53,30 @@ def test_traffic_record_from_ncu_csv(tmp_path, monkeypatch):
     assert rec["launches"] == 2
     assert abs(rec["dram_bytes_per_launch"] - 87.96e6) < 1.0
     assert bench.profiled_traffic("v2lite_c4r4_b32_h16_t8k") == rec["dram_bytes_per_launch"]
+
+
+def test_traffic_record_keyed_by_its_own_kernel_sources(tmp_path, monkeypatch):
+    """A traffic record holds while the sources of its own kernel are unchanged: an edit of the
+    64-head kernel's file leaves a 16-head record valid and voids a 64-head one; an edit of a
+    shared header voids both."""
+    import json
+    import shutil
+
+    import bench
+    csrc = tmp_path / "r" / "bit_mla_kv_qcache_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in ("decode.cu", "decode_tc.cu", "kernels.cuh", "ptx.cuh"):
+        shutil.copy(os.path.join(bench.ROOT, "bit_mla_kv_qcache_gb300", "csrc", f), csrc / f)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path / "r"))
+    monkeypatch.setattr(bench, "traffic_path", lambda w: str(tmp_path / f"traffic_{w}.json"))
+    for w, k in (("h16", "decode_kernel"), ("h64", "decode_tc_kernel")):
+        with open(bench.traffic_path(w), "w") as fh:
+            json.dump({"kernel_regex": k, "dram_bytes_per_launch": 1.0, "source_sha": bench.source_sha(k)}, fh)
+    assert bench.source_sha("decode_kernel") != bench.source_sha("decode_tc_kernel")
+    assert bench.profiled_traffic("h16") == 1.0 and bench.profiled_traffic("h64") == 1.0
+    with open(csrc / "decode_tc.cu", "a") as fh:
+        fh.write("\n// edited\n")
+    assert bench.profiled_traffic("h16") == 1.0 and bench.profiled_traffic("h64") is None
+    with open(csrc / "ptx.cuh", "a") as fh:
+        fh.write("\n// edited\n")
+    assert bench.profiled_traffic("h16") is None
